@@ -1,0 +1,211 @@
+"""ctypes binding of the C ABI in include/attn.h — argument marshalling only.
+
+Every computation happens in the library's CUDA kernels; this module turns
+torch tensors into pointers and strides, fills the parameter structs, calls
+the entry points and raises on a non-OK status. There is no fallback: if the
+shared library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libattn_gb300.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_ALIGN = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_TIMEOUT = -5
+ATTN_ERR_WORKSPACE = -6
+ATTN_BF16 = 0
+ATTN_F32 = 1
+
+STATUS_NAMES = {
+    ATTN_OK: "ATTN_OK", ATTN_ERR_INVALID: "ATTN_ERR_INVALID", ATTN_ERR_UNSUPPORTED: "ATTN_ERR_UNSUPPORTED",
+    ATTN_ERR_ALIGN: "ATTN_ERR_ALIGN", ATTN_ERR_CUDA: "ATTN_ERR_CUDA", ATTN_ERR_TIMEOUT: "ATTN_ERR_TIMEOUT",
+    ATTN_ERR_WORKSPACE: "ATTN_ERR_WORKSPACE",
+}
+
+# every symbol include/attn.h declares
+EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status", "attn_last_error",
+            "attn_set_wait_timeout_ns", "attn_debug_set_producer_stall", "attn_version")
+
+_i64x3 = ctypes.c_int64 * 3
+
+
+class FwdParams(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("N", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("causal", ctypes.c_int32), ("scale", ctypes.c_float),
+        ("reserved0", ctypes.c_int32),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("o", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("q_stride", _i64x3), ("k_stride", _i64x3), ("v_stride", _i64x3), ("o_stride", _i64x3),
+        ("mask", ctypes.c_void_p), ("mask_stride", _i64x3),
+    ]
+
+
+class BwdParams(ctypes.Structure):
+    _fields_ = [
+        ("fwd", FwdParams),
+        ("dout", ctypes.c_void_p), ("do_stride", _i64x3),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("dq_stride", _i64x3), ("dk_stride", _i64x3), ("dv_stride", _i64x3),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"attention library not built ({LIB_PATH}); run `python -m attn_fwd_03_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    lib.attn_fwd.argtypes = [ctypes.POINTER(FwdParams), ctypes.c_void_p]
+    lib.attn_fwd.restype = ctypes.c_int
+    lib.attn_bwd.argtypes = [ctypes.POINTER(BwdParams), ctypes.c_void_p]
+    lib.attn_bwd.restype = ctypes.c_int
+    lib.attn_bwd_workspace_size.argtypes = [ctypes.POINTER(FwdParams)]
+    lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.attn_status.argtypes = [ctypes.c_void_p]
+    lib.attn_status.restype = ctypes.c_int
+    lib.attn_last_error.argtypes = []
+    lib.attn_last_error.restype = ctypes.c_char_p
+    lib.attn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+    lib.attn_set_wait_timeout_ns.restype = None
+    lib.attn_debug_set_producer_stall.argtypes = [ctypes.c_int32]
+    lib.attn_debug_set_producer_stall.restype = None
+    lib.attn_version.argtypes = []
+    lib.attn_version.restype = ctypes.c_int32
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, lib.attn_last_error().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _strides3(t: torch.Tensor):
+    s = t.stride()
+    return _i64x3(s[0], s[1], s[2])
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return ATTN_BF16
+    if t == torch.float32:
+        return ATTN_F32
+    raise TypeError(f"unsupported dtype {t}")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def fwd_params(q, k, v, o, lse, scale: float, causal: bool, mask: Optional[torch.Tensor]) -> FwdParams:
+    """Fill the forward struct from [B, H, N, d] tensors (last dim contiguous)."""
+    B, H, N, d = q.shape
+    p = FwdParams()
+    p.B, p.H, p.N, p.d = B, H, N, d
+    p.dtype = _dtype_code(q.dtype)
+    p.causal = int(bool(causal))
+    p.scale = float(scale)
+    p.reserved0 = 0
+    p.q, p.k, p.v, p.o, p.lse = _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse)
+    p.q_stride, p.k_stride = _strides3(q), _strides3(k)
+    p.v_stride, p.o_stride = _strides3(v), _strides3(o)
+    if mask is not None:
+        m = mask.expand(B, H, N, N)
+        p.mask = m.data_ptr()
+        p.mask_stride = _strides3(m)
+    else:
+        p.mask = None
+        p.mask_stride = _i64x3(0, 0, 0)
+    return p
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Optional[float] = None,
+             causal: bool = False, mask: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O and LSE of exact attention; inputs [B, H, N, d] on the GPU."""
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    p = fwd_params(q, k, v, out, lse, scale, causal, mask)
+    _check(lib.attn_fwd(ctypes.byref(p), ctypes.c_void_p(_stream_handle(stream))))
+    return out, lse
+
+
+def bwd_workspace_size(q: torch.Tensor) -> int:
+    B, H, N, d = q.shape
+    p = FwdParams()
+    p.B, p.H, p.N, p.d = B, H, N, d
+    return int(lib.attn_bwd_workspace_size(ctypes.byref(p)))
+
+
+def attn_bwd(q, k, v, o, lse, dout, *, scale: Optional[float] = None, causal: bool = False,
+             mask: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of sum(dout * O) by recomputation from O and LSE."""
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
+    dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
+    dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
+    need = bwd_workspace_size(q)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    bp = BwdParams()
+    bp.fwd = fwd_params(q, k, v, o, lse, scale, causal, mask)
+    bp.dout, bp.do_stride = _ptr(dout), _strides3(dout)
+    bp.dq, bp.dk, bp.dv = _ptr(dq), _ptr(dk), _ptr(dv)
+    bp.dq_stride, bp.dk_stride, bp.dv_stride = _strides3(dq), _strides3(dk), _strides3(dv)
+    bp.workspace = workspace.data_ptr()
+    bp.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.attn_bwd(ctypes.byref(bp), ctypes.c_void_p(_stream_handle(stream))))
+    return dq, dk, dv
+
+
+def attn_status(stream=None) -> int:
+    """Synchronize and return the status code (does not raise)."""
+    return int(lib.attn_status(ctypes.c_void_p(_stream_handle(stream))))
+
+
+def last_error() -> str:
+    return lib.attn_last_error().decode(errors="replace")
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib.attn_set_wait_timeout_ns(int(ns))
+
+
+def debug_set_producer_stall(kv_tiles: int) -> None:
+    lib.attn_debug_set_producer_stall(int(kv_tiles))
+
+
+def version() -> int:
+    return int(lib.attn_version())

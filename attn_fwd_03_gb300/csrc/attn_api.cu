@@ -1,0 +1,288 @@
+// attn_api.cu — the C ABI (include/attn.h): argument checks, the device error
+// word, TMA tensor-map construction and kernel launches.
+//
+// Nothing here allocates device memory. Argument errors are detected before
+// any launch and returned with a message (attn_last_error); in-kernel errors
+// (a bounded wait that ran out) land in a per-device error word that
+// attn_status() reads and clears.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace attn {
+
+__device__ int g_error_word;  // one per device; ATTN_ERR_TIMEOUT when a kernel gave up
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+thread_local int32_t t_stall_after = 0;
+uint64_t g_timeout_ns = 2000000000ull;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+attn_status_t fail(attn_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+attn_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device error word address and SM count of the current device, set up once.
+attn_status_t device_setup(LaunchCommon* lc) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_err_ptr[dev] = static_cast<int*>(p);
+        g_num_sms[dev] = sms;
+    }
+    lc->err = g_err_ptr[dev];
+    lc->num_sms = g_num_sms[dev];
+    lc->timeout_ns = g_timeout_ns;
+    lc->stall_after = t_stall_after;
+    return ATTN_OK;
+}
+
+size_t elem_size(int32_t dtype) { return dtype == ATTN_F32 ? 4 : 2; }
+
+bool misaligned_ptr(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+attn_status_t check_tensor(const char* name, const void* ptr, const int64_t* st, size_t es, bool allow_zero) {
+    if (!ptr) return fail(ATTN_ERR_INVALID, "%s is NULL", name);
+    for (int i = 0; i < 3; ++i) {
+        if (st[i] < 0 || (!allow_zero && st[i] == 0))
+            return fail(ATTN_ERR_INVALID, "%s stride[%d] = %lld is not positive", name, i, (long long)st[i]);
+        if (((uint64_t)st[i] * es) % 16 != 0)
+            return fail(ATTN_ERR_ALIGN, "%s stride[%d] = %lld elements is not a multiple of 16 bytes", name, i,
+                        (long long)st[i]);
+        if ((uint64_t)st[i] * es >= (1ull << 40))
+            return fail(ATTN_ERR_UNSUPPORTED, "%s stride[%d] too large", name, i);
+    }
+    if (misaligned_ptr(ptr)) return fail(ATTN_ERR_ALIGN, "%s is not 16-byte aligned", name);
+    return ATTN_OK;
+}
+
+// Checks shared by forward and backward. *empty = nothing to compute.
+attn_status_t check_fwd(const attn_fwd_params* p, bool* empty) {
+    if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
+    if (p->B < 0 || p->H < 0 || p->N < 0)
+        return fail(ATTN_ERR_INVALID, "negative size B=%d H=%d N=%d", p->B, p->H, p->N);
+    if (p->dtype != ATTN_BF16 && p->dtype != ATTN_F32) return fail(ATTN_ERR_INVALID, "unknown dtype %d", p->dtype);
+    if (p->causal != 0 && p->causal != 1) return fail(ATTN_ERR_INVALID, "causal must be 0 or 1, got %d", p->causal);
+    if (p->reserved0 != 0) return fail(ATTN_ERR_INVALID, "reserved0 must be 0");
+    if (!std::isfinite(p->scale) || !(p->scale > 0.f))
+        return fail(ATTN_ERR_INVALID, "scale must be positive and finite");
+    if (p->d != 64 && p->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not built (64 or 128)", p->d);
+    if (p->B > 65535 || p->H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B and H are limited to 65535");
+    *empty = (p->B == 0 || p->H == 0 || p->N == 0);
+    if (*empty) return ATTN_OK;
+    const size_t es = elem_size(p->dtype);
+    attn_status_t st;
+    if ((st = check_tensor("q", p->q, p->q_stride, es, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("k", p->k, p->k_stride, es, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("v", p->v, p->v_stride, es, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("o", p->o, p->o_stride, es, false)) != ATTN_OK) return st;
+    if (!p->lse) return fail(ATTN_ERR_INVALID, "lse is NULL");
+    if (misaligned_ptr(p->lse)) return fail(ATTN_ERR_ALIGN, "lse is not 16-byte aligned");
+    if (p->mask && (st = check_tensor("mask", p->mask, p->mask_stride, es, true)) != ATTN_OK) return st;
+    if (p->mask && p->mask_stride[2] == 0 && p->N > 1)
+        return fail(ATTN_ERR_INVALID, "mask row stride must be positive");
+    return ATTN_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+attn_status_t get_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return ATTN_OK;
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return ATTN_OK;
+}
+
+// 4-D bf16 map over (col, row, h, b) with a 64 x box_rows box and the 128-byte
+// swizzle: one box is box_rows rows of 128 bytes.
+attn_status_t encode_bf16_map(CUtensorMap* m, const char* name, const void* base, uint64_t cols, uint64_t rows,
+                              uint64_t hs, uint64_t bs, const int64_t* st, uint32_t box_rows) {
+    cuuint64_t dims[4] = {cols, rows, hs, bs};
+    cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+    // a dimension of extent 1 may carry stride 0 (broadcast); give it a legal one
+    for (int i = 0; i < 3; ++i)
+        if (strides[i] == 0) strides[i] = 16;
+    cuuint32_t box[4] = {64, box_rows, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+    return ATTN_OK;
+}
+
+attn_status_t build_fwd_maps(const attn_fwd_params& p, FwdMaps* m) {
+    attn_status_t st = get_encoder();
+    if (st != ATTN_OK) return st;
+    const uint64_t N = (uint64_t)p.N, d = (uint64_t)p.d;
+    if ((st = encode_bf16_map(&m->q, "q", p.q, d, N, p.H, p.B, p.q_stride, 128)) != ATTN_OK) return st;
+    if ((st = encode_bf16_map(&m->k, "k", p.k, d, N, p.H, p.B, p.k_stride, 128)) != ATTN_OK) return st;
+    if ((st = encode_bf16_map(&m->v, "v", p.v, d, N, p.H, p.B, p.v_stride, 128)) != ATTN_OK) return st;
+    if ((st = encode_bf16_map(&m->o, "o", p.o, d, N, p.H, p.B, p.o_stride, 128)) != ATTN_OK) return st;
+    if (p.mask) {
+        const uint64_t hm = p.mask_stride[1] != 0 ? (uint64_t)p.H : 1;
+        const uint64_t bm = p.mask_stride[0] != 0 ? (uint64_t)p.B : 1;
+        if ((st = encode_bf16_map(&m->mask, "mask", p.mask, N, N, hm, bm, p.mask_stride, 128)) != ATTN_OK)
+            return st;
+    } else {
+        m->mask = m->q;  // unused by the kernel variant without a mask
+    }
+    return ATTN_OK;
+}
+
+attn_status_t build_bwd_maps(const attn_bwd_params& p, BwdMaps* m) {
+    FwdMaps f;
+    attn_status_t st = build_fwd_maps(p.fwd, &f);
+    if (st != ATTN_OK) return st;
+    m->q = f.q;
+    m->k = f.k;
+    m->v = f.v;
+    m->mask = f.mask;
+    const uint64_t N = (uint64_t)p.fwd.N, d = (uint64_t)p.fwd.d;
+    return encode_bf16_map(&m->dout, "dout", p.dout, d, N, p.fwd.H, p.fwd.B, p.do_stride, 128);
+}
+
+}  // namespace
+
+static size_t stats_bytes(const attn_fwd_params& p) {
+    const size_t tiles = (size_t)p.B * p.H * (((size_t)p.N + 127) / 128);
+    return tiles * 2 * 128 * sizeof(float);  // a multiple of 1024
+}
+
+size_t bwd_workspace_bytes(const attn_fwd_params& p) {
+    const size_t rows = (size_t)p.B * p.H * p.N;
+    if (rows == 0) return 0;
+    return stats_bytes(p) + rows * (size_t)p.d * sizeof(float);
+}
+
+BwdWorkspace bwd_workspace_split(const attn_bwd_params& p) {
+    char* base = static_cast<char*>(p.workspace);
+    return BwdWorkspace{reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + stats_bytes(p.fwd))};
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status_t attn_fwd(const attn_fwd_params* p, void* stream) {
+    bool empty = false;
+    attn_status_t st = check_fwd(p, &empty);
+    if (st != ATTN_OK || empty) return st;
+    LaunchCommon lc;
+    if ((st = device_setup(&lc)) != ATTN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (p->dtype == ATTN_F32) {
+        e = launch_fwd_simt(*p, s);
+    } else {
+        FwdMaps maps;
+        if ((st = build_fwd_maps(*p, &maps)) != ATTN_OK) return st;
+        e = launch_fwd_tc(*p, maps, lc, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
+    return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_size(const attn_fwd_params* p) {
+    if (!p || p->B < 0 || p->H < 0 || p->N < 0 || (p->d != 64 && p->d != 128)) return 0;
+    return bwd_workspace_bytes(*p);
+}
+
+attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
+    if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
+    bool empty = false;
+    attn_status_t st = check_fwd(&p->fwd, &empty);
+    if (st != ATTN_OK) return st;
+    if (p->fwd.dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 only");
+    if (empty) return ATTN_OK;
+    if ((st = check_tensor("dout", p->dout, p->do_stride, 2, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("dq", p->dq, p->dq_stride, 2, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("dk", p->dk, p->dk_stride, 2, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("dv", p->dv, p->dv_stride, 2, false)) != ATTN_OK) return st;
+    const size_t need = bwd_workspace_bytes(p->fwd);
+    if (!p->workspace || p->workspace_bytes < need)
+        return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", p->workspace_bytes, need);
+    if ((reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)
+        return fail(ATTN_ERR_ALIGN, "workspace is not 256-byte aligned");
+    LaunchCommon lc;
+    if ((st = device_setup(&lc)) != ATTN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const BwdWorkspace ws = bwd_workspace_split(*p);
+    BwdMaps maps;
+    if ((st = build_bwd_maps(*p, &maps)) != ATTN_OK) return st;
+    cudaError_t e = launch_bwd_prepass(*p, ws, lc.err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd pre-pass launch");
+    e = launch_bwd_tc(*p, maps, ws, lc, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd main launch");
+    e = launch_bwd_dq_finalize(*p, ws, lc.err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dQ finalize launch");
+    return ATTN_OK;
+}
+
+attn_status_t attn_status(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "asynchronous CUDA error");
+    LaunchCommon lc;
+    attn_status_t st = device_setup(&lc);
+    if (st != ATTN_OK) return st;
+    int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+        if (word == ATTN_ERR_TIMEOUT) return fail(ATTN_ERR_TIMEOUT, "a kernel's bounded wait ran out");
+        if (word == -7) return fail(ATTN_ERR_CUDA, "a kernel skipped a misaligned access or buffer");
+        return fail(ATTN_ERR_CUDA, "device error word %d", word);
+    }
+    return ATTN_OK;
+}
+
+const char* attn_last_error(void) { return t_last_error; }
+
+void attn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns < 1000000ull ? 1000000ull : ns; }
+
+void attn_debug_set_producer_stall(int32_t kv_tiles) { t_stall_after = kv_tiles > 0 ? kv_tiles : 0; }
+
+int32_t attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,433 @@
+// attn_bwd_sm103.cu — bf16 attention backward on the sm_103a tensor cores.
+//
+// The backward pass recomputes the score and probability tiles from Q, K, V,
+// the saved per-row log-sum-exp and D = rowsum(dO * O), instead of storing
+// the N x N probabilities ("What is FlashAttention?", Step 4; "FlashAttention",
+// "What it does not do"). Per (b, h) the gradients are the textbook ones:
+//     P = exp(scale * Q K^T + mask - LSE),   dV = P^T dO,   dP = dO V^T,
+//     dS = P * (dP - D),   dK = scale * dS^T Q,   dQ = scale * dS K.
+//
+// One CTA owns a 128-key tile of one (b, h) and keeps K, V and the fp32 dK,
+// dV accumulators on chip while 128-query tiles stream past (query tiles that
+// lie entirely above the causal diagonal are never visited). Per query tile:
+//   S^T = K Q^T and dP^T = V dO^T      (tcgen05, both operands in shared memory)
+//   P^T, dS^T (one thread per key row)  bf16 into tensor memory, dS also into
+//                                      shared memory (swizzled, query-contiguous)
+//   dV += P^T dO, dK += dS^T Q         (tcgen05, A operand in tensor memory)
+//   dQ_tile = dS K                     (tcgen05, A = dS read query-major)
+// and a second warpgroup adds scale * dQ_tile into the fp32 dQ accumulator in
+// global memory with vector reductions (other key tiles add to the same rows).
+//
+// Warp roles (12 warps):
+//   warps 0-3   P^T / dS^T from the score tiles (thread = key row), then the
+//               dK / dV epilogue
+//   warps 4-7   dQ drain (thread = query row of the tile)
+//   warp  8     TMA producer: K and V once, then per query tile Q_i, dO_i, the
+//               mask tile and the tile's -LSE*log2(e) and D statistics (1 KB,
+//               written tile-padded by the pre-pass)
+//   warp  9     TMEM allocator and MMA issuer
+//   warps 10-11 idle
+//
+// Tensor memory (512 columns, lane = key row for S^T/dP^T/dK/dV, query row for dQ):
+//   [0,128)    S^T fp32; P^T bf16 pairs in [0,64); dQ columns 0-63 in [64,128)
+//   [128,256)  dP^T fp32; dS^T bf16 pairs in [128,192); dQ columns 64-127 in [192,256)
+//   [256,256+D)      dV accumulator
+//   [256+D,256+2D)   dK accumulator
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+using namespace ptx;
+
+constexpr int BQ = 128;  // query rows per tile
+constexpr int BK = 128;  // key rows per CTA
+
+template <int D, bool MASK>
+struct BwdCfg {
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kMaskBytes = BQ * BK * 2;
+    static constexpr int kStages = (D == 128 && MASK) ? 1 : 2;
+    static constexpr int kVecOffInStage = 2 * kTileBytes + (MASK ? kMaskBytes : 0);
+    static constexpr int kStageBytes = kVecOffInStage + 1024;  // + [-LSE*log2e | D] x 128
+    static constexpr int kThreads = 384;
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kKOff + kTileBytes;
+    static constexpr int kDSOff = kVOff + kTileBytes;
+    static constexpr int kStageOff = kDSOff + BQ * BK * 2;
+    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kSmemBytes = kBarOff + 256;
+    static constexpr uint32_t kIdescS = idesc_bf16(BK, BQ, false, false);   // S^T, dP^T
+    static constexpr uint32_t kIdescKV = idesc_bf16(BK, D, false, true);    // dV, dK (A in TMEM)
+    static constexpr uint32_t kIdescQ = idesc_bf16(BQ, 64, true, true);     // dQ half (A = dS query-major)
+};
+
+struct BwdParamsDev {
+    int B, H, N;
+    int causal;
+    float c;      // scale * log2(e)
+    float scale;
+    const float* stats;  // [B*H][nq][2][128]: -LSE*log2e, then D
+    float* dq_acc;
+    __nv_bfloat16 *dk, *dv;
+    long long dk_sb, dk_sh, dk_sn, dv_sb, dv_sh, dv_sn;
+    int mask_hb, mask_bb;
+    int n_ktiles;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+struct __align__(8) BwdBarriers {
+    uint64_t kv_full;
+    uint64_t st_full[2], st_empty[2];
+    uint64_t s_full, ds_ready, dq_full, dq_empty, kv_done;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+    return sdesc_sw128(tile + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+    return sdesc_sw128(tile + kk * (16 * 128), 128 * 128, 1024);
+}
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint32_t a = smem_u32(bar);
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(a, parity))
+        if (globaltimer() - t0 > timeout_ns) break;
+}
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+template <int D, bool MASK>
+__global__ void __launch_bounds__(384, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_mask, const BwdParamsDev p) {
+    using Cfg = BwdCfg<D, MASK>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    BwdBarriers& bar = *reinterpret_cast<BwdBarriers*>(smem + Cfg::kBarOff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    WaitCtl wc{p.err, &bar.abort_flag, p.timeout_ns};
+
+    // work unit: key tile kt of (b, h); early key tiles first (they see the most query tiles)
+    const int bh = p.B * p.H;
+    const int kt = blockIdx.x / bh;
+    const int b = (blockIdx.x % bh) / p.H, h = blockIdx.x % p.H;
+    const int k0 = kt * BK;
+    const int nq_all = (p.N + BQ - 1) / BQ;
+    const int i_begin = p.causal ? kt : 0;  // first query tile on or below the diagonal
+    const int n_it = nq_all - i_begin;
+
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicExch(p.err, -7);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        bar.abort_flag = 0;
+        mbar_init(&bar.kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar.st_full[s], 1);
+            mbar_init(&bar.st_empty[s], 1);
+        }
+        mbar_init(&bar.s_full, 1);
+        mbar_init(&bar.ds_ready, 128);
+        mbar_init(&bar.dq_full, 1);
+        mbar_init(&bar.dq_empty, 128);
+        mbar_init(&bar.kv_done, 1);
+        mbar_init(&bar.drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&bar.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_base;
+    const uint32_t sK = smem_u32(smem + Cfg::kKOff), sV = smem_u32(smem + Cfg::kVOff);
+    const uint32_t sDS = smem_u32(smem + Cfg::kDSOff);
+
+    if (warp == 8) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(&bar.kv_full, 2 * Cfg::kTileBytes);
+            for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
+                tma_load_4d(smem + Cfg::kKOff + bx * 128 * 128, &tm_k, &bar.kv_full, bx * 64, k0, h, b);
+                tma_load_4d(smem + Cfg::kVOff + bx * 128 * 128, &tm_v, &bar.kv_full, bx * 64, k0, h, b);
+            }
+            const int hm = p.mask_hb ? h : 0, bm = p.mask_bb ? b : 0;
+            bool ok = true;
+            int it = 0;
+            for (; it < n_it && ok; ++it) {
+                const int s = it % Cfg::kStages;
+                ok = mbar_wait(&bar.st_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
+                if (!ok) break;
+                const int q0 = (i_begin + it) * BQ;
+                uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+                mbar_arrive_expect_tx(&bar.st_full[s], Cfg::kStageBytes);
+                for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
+                    tma_load_4d(st + bx * 128 * 128, &tm_q, &bar.st_full[s], bx * 64, q0, h, b);
+                    tma_load_4d(st + Cfg::kTileBytes + bx * 128 * 128, &tm_do, &bar.st_full[s], bx * 64, q0, h, b);
+                }
+                if (MASK)
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_4d(st + 2 * Cfg::kTileBytes + bx * 128 * 128, &tm_mask, &bar.st_full[s],
+                                    k0 + bx * 64, q0, hm, bm);
+                bulk_load(st + Cfg::kVecOffInStage,
+                          p.stats + ((long long)(b * p.H + h) * nq_all + (i_begin + it)) * 256, 1024,
+                          &bar.st_full[s]);
+            }
+            const int last = it < Cfg::kStages ? it : Cfg::kStages;
+            for (int i = it - last; i < it; ++i)
+                drain_wait(&bar.st_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
+            drain_wait(&bar.kv_full, 0, p.timeout_ns);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(&bar.kv_full, 0, wc);
+            tc_fence_after();
+            for (int it = 0; it < n_it && ok; ++it) {
+                const int s = it % Cfg::kStages;
+                ok = mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+                if (!ok) break;
+                if (it > 0) {  // S^T / dP^T overwrite the previous dQ tile
+                    ok = mbar_wait(&bar.dq_empty, (it - 1) & 1, wc);
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes);
+                const uint32_t sdO = sQ + Cfg::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 0, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+                mma_commit(&bar.s_full);
+                ok = mbar_wait(&bar.ds_ready, it & 1, wc);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    mma_ts(tmem + 256, tmem + kk * 8, mnmajor_desc(sdO, kk), Cfg::kIdescKV,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    mma_ts(tmem + 256 + D, tmem + 128 + kk * 8, mnmajor_desc(sQ, kk), Cfg::kIdescKV,
+                           (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int half = 0; half < D / 64; ++half)
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_ss(tmem + (half == 0 ? 64 : 192), mnmajor_desc(sDS, kk),
+                               mnmajor_desc(sK + half * 128 * 128, kk), Cfg::kIdescQ, kk > 0 ? 1u : 0u);
+                mma_commit(&bar.dq_full);
+                mma_commit(&bar.st_empty[s]);
+            }
+            if (ok) mma_commit(&bar.kv_done);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mma_commit(&bar.drain);
+            drain_wait(&bar.drain, 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------ P^T, dS^T (thread = key row)
+        const int kr = warp * 32 + lane;
+        const int kg = k0 + kr;
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t tRow = tmem + lane_off;
+        uint8_t* ds_row = smem + Cfg::kDSOff + kr * 128;
+        bool ok = true;
+        for (int it = 0; it < n_it && ok; ++it) {
+            const int q0 = (i_begin + it) * BQ;
+            const int s = it % Cfg::kStages;
+            ok = mbar_wait(&bar.s_full, it & 1, wc);
+            // the stage's statistics (and mask tile) are visible once its copies completed
+            ok = ok && mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const uint8_t* stage = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+            const float* nlv = reinterpret_cast<const float*>(stage + Cfg::kVecOffInStage);
+            const float* ddv = nlv + 128;
+            tc_fence_after();
+            const bool diag = p.causal && (q0 == k0);
+            const bool key_ok = kg < p.N;
+            const uint8_t* mt = stage + 2 * Cfg::kTileBytes;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], pv[32];
+                tmem_ld32(tRow + 32 * c, sv);
+                tmem_ld32(tRow + 128 + 32 * c, pv);
+                tmem_wait_ld();
+                uint32_t pk[16], dk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float pp[2], dd2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int q = 32 * c + i + e;
+                        float x = __uint_as_float(sv[i + e]) * p.c + nlv[q];
+                        if (MASK) {
+                            const int kb = kr >> 6, kc = (kr & 63) >> 3;
+                            const __nv_bfloat16 mv = *reinterpret_cast<const __nv_bfloat16*>(
+                                mt + kb * 128 * 128 + q * 128 + ((kc ^ (q & 7)) << 4) + (kr & 7) * 2);
+                            x += __bfloat162float(mv) * kLog2e;
+                        }
+                        if (!key_ok || (diag && q < kr)) x = -INFINITY;
+                        const float pr = ex2(x);
+                        pp[e] = pr;
+                        dd2[e] = pr * (__uint_as_float(pv[i + e]) - ddv[q]);
+                    }
+                    pk[i / 2] = pack_bf16(pp[0], pp[1]);
+                    dk[i / 2] = pack_bf16(dd2[0], dd2[1]);
+                }
+                tmem_st16(tRow + 16 * c, pk);
+                tmem_st16(tRow + 128 + 16 * c, dk);
+                // dS row kr, queries 32c .. 32c+31 -> box (32c / 64), chunks ((32c % 64) / 8) .. +3
+                uint8_t* box = ds_row + ((32 * c) >> 6) * (128 * 128);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int ch = ((32 * c) & 63) / 8 + j;
+                    *reinterpret_cast<uint4*>(box + ((ch ^ (kr & 7)) << 4)) =
+                        make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar.ds_ready);
+        }
+        // epilogue: dV and scale * dK rows of this key tile
+        if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            __nv_bfloat16* dvr = p.dv + b * p.dv_sb + h * p.dv_sh + (long long)kg * p.dv_sn;
+            __nv_bfloat16* dkr = p.dk + b * p.dk_sb + h * p.dk_sh + (long long)kg * p.dk_sn;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                __nv_bfloat16* dst_row = which == 0 ? dvr : dkr;
+                const float mul = which == 0 ? 1.f : p.scale;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tRow + 256 + which * D + c0, v);
+                    tmem_wait_ld();
+                    if (kg < p.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(
+                                pack_bf16(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                                pack_bf16(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
+                                pack_bf16(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
+                                pack_bf16(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+                    }
+                }
+            }
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------ dQ drain (thread = query row)
+        const int qr = (warp - 4) * 32 + lane;
+        const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+        bool ok = true;
+        for (int it = 0; it < n_it && ok; ++it) {
+            ok = mbar_wait(&bar.dq_full, it & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[D];
+            tmem_ld32_at<0>(tmem + lane_off + 64, v);
+            tmem_ld32_at<32>(tmem + lane_off + 96, v);
+            if constexpr (D == 128) {
+                tmem_ld32_at<64>(tmem + lane_off + 192, v);
+                tmem_ld32_at<96>(tmem + lane_off + 224, v);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bar.dq_empty);
+            const int qg = (i_begin + it) * BQ + qr;
+            if (qg < p.N) {
+                float* dst = p.dq_acc + (((long long)b * p.H + h) * p.N + qg) * D;
+#pragma unroll
+                for (int c = 0; c < D; c += 4)
+                    red_add_v4(dst + c, __uint_as_float(v[c]) * p.scale, __uint_as_float(v[c + 1]) * p.scale,
+                               __uint_as_float(v[c + 2]) * p.scale, __uint_as_float(v[c + 3]) * p.scale);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+template <int D, bool MASK>
+cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, const BwdWorkspace& ws,
+                            const LaunchCommon& lc, cudaStream_t s) {
+    using Cfg = BwdCfg<D, MASK>;
+    static_assert(Cfg::kSmemBytes <= 232448, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const attn_fwd_params& f = prm.fwd;
+    BwdParamsDev p{};
+    p.B = f.B;
+    p.H = f.H;
+    p.N = f.N;
+    p.causal = f.causal;
+    p.c = f.scale * kLog2e;
+    p.scale = f.scale;
+    p.stats = ws.stats;
+    p.dq_acc = ws.dq_acc;
+    p.dk = static_cast<__nv_bfloat16*>(prm.dk);
+    p.dv = static_cast<__nv_bfloat16*>(prm.dv);
+    p.dk_sb = prm.dk_stride[0];
+    p.dk_sh = prm.dk_stride[1];
+    p.dk_sn = prm.dk_stride[2];
+    p.dv_sb = prm.dv_stride[0];
+    p.dv_sh = prm.dv_stride[1];
+    p.dv_sn = prm.dv_stride[2];
+    p.mask_hb = f.mask ? (f.mask_stride[1] != 0) : 0;
+    p.mask_bb = f.mask ? (f.mask_stride[0] != 0) : 0;
+    p.n_ktiles = (f.N + BK - 1) / BK;
+    p.err = lc.err;
+    p.timeout_ns = lc.timeout_ns;
+    const unsigned grid = (unsigned)(p.n_ktiles * f.B * f.H);
+    bwd_tc_kernel<D, MASK><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(maps.q, maps.k, maps.v, maps.dout,
+                                                                        maps.mask, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const attn_bwd_params& p, const BwdMaps& maps, const BwdWorkspace& ws,
+                          const LaunchCommon& lc, cudaStream_t s) {
+    const bool mask = p.fwd.mask != nullptr;
+    if (p.fwd.d == 64)
+        return mask ? launch_bwd_tc_t<64, true>(p, maps, ws, lc, s) : launch_bwd_tc_t<64, false>(p, maps, ws, lc, s);
+    return mask ? launch_bwd_tc_t<128, true>(p, maps, ws, lc, s) : launch_bwd_tc_t<128, false>(p, maps, ws, lc, s);
+}
+
+}  // namespace attn

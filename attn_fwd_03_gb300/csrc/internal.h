@@ -1,0 +1,58 @@
+// internal.h — declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// What every launch needs besides the problem itself.
+struct LaunchCommon {
+    int* err;             // device error word of the current device
+    uint64_t timeout_ns;  // bound on any single in-kernel wait
+    int32_t stall_after;  // test hook: load warp stops after this many K/V tiles (0 = off)
+    int num_sms;          // SM count of the current device
+};
+
+// Tensor maps for the tcgen05 forward (built by the host API).
+struct FwdMaps {
+    CUtensorMap q, k, v, o, mask;
+};
+
+// Tensor maps for the tcgen05 backward.
+struct BwdMaps {
+    CUtensorMap q, k, v, dout, mask;
+};
+
+// The two parts of the backward workspace.
+//  stats:  per (b, h) and 128-row query tile, 128 values of -LSE * log2(e)
+//          (-inf for fully masked rows and padding rows) followed by 128 values
+//          of D = rowsum(dO * O); fp32 [B*H][ceil(N/128)][2][128]
+//  dq_acc: fp32 [B, H, N, d] dQ accumulator (already multiplied by the scale)
+struct BwdWorkspace {
+    float* stats;
+    float* dq_acc;
+};
+size_t bwd_workspace_bytes(const attn_fwd_params& p);
+BwdWorkspace bwd_workspace_split(const attn_bwd_params& p);
+
+// attn_fwd_sm103.cu — tcgen05 forward (bf16).
+cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);
+
+// attn_bwd_sm103.cu — tcgen05 backward main kernel (bf16).
+cudaError_t launch_bwd_tc(const attn_bwd_params& p, const BwdMaps& maps, const BwdWorkspace& ws,
+                          const LaunchCommon& lc, cudaStream_t s);
+
+// attn_simt.cu — CUDA-core kernels.
+cudaError_t launch_fwd_simt(const attn_fwd_params& p, cudaStream_t s);  // fp32 inputs
+cudaError_t launch_bwd_prepass(const attn_bwd_params& p, const BwdWorkspace& ws, int* err, cudaStream_t s);
+cudaError_t launch_bwd_dq_finalize(const attn_bwd_params& p, const BwdWorkspace& ws, int* err, cudaStream_t s);
+
+}  // namespace attn

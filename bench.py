@@ -1,0 +1,341 @@
+"""Benchmark: exact tiled attention forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+attn_fwd (O, LSE) then attn_bwd (D pre-pass, recompute kernel, dQ finalize)
+on the workload's tensors, already resident in device memory. The default
+workload is B=4 H=16 N=2048 d=64 bf16 causal forward + backward.
+
+Throughput is useful attention FLOPs per second: 4 B H N^2 d per forward,
+2.5x that per backward, halved for causal ("FlashAttention", "Checking it on
+a real system"). Prints ONE JSON line on rank 0.
+
+Timing: W untimed warm-up steps, then K timed steps between a barrier and a
+device synchronize. Inputs of the default workload fit in L2, so a 256 MiB
+buffer is rewritten before every step (outside the per-step events); each
+step's fwd and bwd are bracketed by CUDA events on the launching stream.
+Under torchrun every rank runs its own replica (weak scaling) and the max
+over ranks is reported; nothing crosses ranks except the timing reduction.
+
+--impl reference times the fp64 CPU oracle instead, on a bounded sample of
+the same workload, on rank 0's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# our kernels per step: forward 1, backward 3 (pre-pass, main, dQ finalize) in the
+# tensor-core path; the CUDA-core backward splits its main kernel in two
+LAUNCHES_FWD = 1
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def step_flops(w: W.Workload, backward: bool = True) -> float:
+    f = W.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    if backward and w.backward:
+        f += W.attention_flops(w.B, w.H, w.N, w.d, w.causal, backward=True)
+    return f
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- oracle arm
+def oracle_sample(w: W.Workload, budget_s: float, max_heads=None):
+    """Time the fp64 oracle (forward + backward) on whole heads until the
+    budget is used; returns (seconds, flops of the sampled heads, heads)."""
+    from oracle import ref
+    import numpy as np
+    inp = W.make_inputs(w, shape=(1, min(w.H, 4), w.N, w.d))
+    q, k, v = (inp[n][0].to(__import__("torch").float64).numpy() for n in ("q", "k", "v"))
+    do = inp["do"][0].to(__import__("torch").float64).numpy() if "do" in inp else None
+    maskh = None if inp.get("mask") is None else inp["mask"][0, 0].to(__import__("torch").float64).numpy()
+    t0 = time.perf_counter()
+    heads = 0
+    while True:
+        h = heads % q.shape[0]
+        ref.forward_head(q[h], k[h], v[h], w.scale, w.causal, maskh)
+        if w.backward and do is not None:
+            ref.backward_head(q[h], k[h], v[h], do[h], w.scale, w.causal, maskh)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_heads and heads >= max_heads):
+            break
+    flops = step_flops(W.Workload(**{**w.__dict__, "B": 1, "H": heads}))
+    return el, flops, heads
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(w, 0.0, max_heads=1)
+    secs, flops = [], []
+    for _ in range(args.steps):
+        el, fl, _ = oracle_sample(w, args.ref_budget, max_heads=None)
+        secs.append(el)
+        flops.append(fl)
+    value = sum(flops) / sum(secs) / 1e12
+    ms = 1000.0 * sum(secs) / len(secs)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "sample": "whole heads of the workload, fp64 oracle forward+backward, "
+                                            f"~{args.ref_budget:.0f} s per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": f"whole heads per step until {args.ref_budget:.0f} s elapsed"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    import attn_fwd_03_gb300 as A
+
+    peaks, peak_kind = load_peaks()
+    inp = W.make_inputs(w)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    mask = inp["mask"].to(dev) if inp.get("mask") is not None else None
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(A.bwd_workspace_size(q), 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        A.attn_fwd(q, k, v, scale=w.scale, causal=w.causal, mask=mask, out=o, lse=lse)
+        A.attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask, dq=dq, dk=dk, dv=dv,
+                   workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if A.attn_status() != A.ATTN_OK:
+        raise RuntimeError(A.last_error())
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            A.attn_fwd(q, k, v, scale=w.scale, causal=w.causal, mask=mask, out=o, lse=lse)
+            ev[i][1].record(stream)
+            A.attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask, dq=dq, dk=dk, dv=dv,
+                       workspace=ws)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    if A.attn_status() != A.ATTN_OK:
+        raise RuntimeError(A.last_error())
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    ms = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / args.steps
+    ms_fwd = sum(fwd_ms) / args.steps
+    ms_bwd = sum(bwd_ms) / args.steps
+    if world > 1:
+        t = torch.tensor([ms, ms_fwd, ms_bwd], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_fwd, ms_bwd = t.tolist()
+
+    f_step = step_flops(w)
+    f_fwd = step_flops(w, backward=False)
+    value = f_step * world / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    fwd_tflops = f_fwd / (ms_fwd * 1e-3) / 1e12
+    bwd_tflops = (f_step - f_fwd) / (ms_bwd * 1e-3) / 1e12
+
+    # ---- end to end through the public API with pinned host buffers
+    h_in = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    h_out = {"o": torch.empty_like(inp["q"]).pin_memory(), "lse": torch.empty(q.shape[:3]).pin_memory(),
+             "dq": torch.empty_like(inp["q"]).pin_memory(), "dk": torch.empty_like(inp["k"]).pin_memory(),
+             "dv": torch.empty_like(inp["v"]).pin_memory()}
+    h_mask = inp["mask"].pin_memory() if inp.get("mask") is not None else None
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values()) + \
+        (h_mask.numel() * h_mask.element_size() if h_mask is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+            dst.copy_(h_in[n], non_blocking=True)
+        if h_mask is not None:
+            mask.copy_(h_mask, non_blocking=True)
+        step()
+        for n, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            h_out[n].copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+    e2e_value = f_step * world / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    launches_bwd = 4 if getattr(A, "BWD_LAUNCHES", None) is None else A.BWD_LAUNCHES
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**w.describe(), "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "256 MiB buffer rewritten before every timed step (inputs fit in L2)",
+                   "step": "attn_fwd + attn_bwd"},
+        "pct_of_peak": 100.0 * value / world / peak,
+        "fwd": {"ms": ms_fwd, "tflops": fwd_tflops, "pct_of_peak": 100.0 * fwd_tflops / peak},
+        "bwd": {"ms": ms_bwd, "tflops": bwd_tflops, "pct_of_peak": 100.0 * bwd_tflops / peak},
+        "roofline": {"bound": "tensor", "kernel": "forward (one launch per attn_fwd)", "achieved": fwd_tflops,
+                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_tflops / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (LAUNCHES_FWD + launches_bwd),
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        el, fl, heads = oracle_sample(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                                "sample": f"{heads} whole head(s) of the workload, fp64 forward+backward, "
+                                          f"{el:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=5.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,152 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * Exact scaled-dot-product attention computed tile by tile with an online
+ * softmax: per query row the kernels carry a running max m, a denominator l
+ * and an output accumulator o, rescaled by exp(m_old - m_new) whenever a new
+ * key tile raises the max, so the N x N score and probability matrices never
+ * reach device memory ("Explain FlashAttention and why it is IO-aware",
+ * "Keep only the state needed for the final weighted average"; "What is
+ * FlashAttention?", Steps 2-3). The backward pass recomputes the score and
+ * probability tiles from Q, K, V, O and the saved per-row log-sum-exp
+ * ("What is FlashAttention?", Step 4; "FlashAttention", "What it does not do").
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors Q, K, V, O (and dO, dQ, dK, dV) are logically [B, H, N, d] with
+ *    the last dimension contiguous; the three strides given for (b, h, n) are
+ *    in ELEMENTS and may describe any permutation of B/H/N (e.g. BHND or
+ *    BNHD). Base pointers and every stride in bytes must be multiples of 16.
+ *  - LSE is float32 [B, H, N], contiguous (row-major).
+ *  - The caller owns all memory. The library allocates no device memory; the
+ *    backward pass uses a caller-provided workspace whose size
+ *    attn_bwd_workspace_size() reports.
+ *  - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream). Argument errors are found on
+ *    the host before anything is launched and are returned directly, with a
+ *    message from attn_last_error(). Errors inside a kernel (a bounded wait
+ *    that ran out) are recorded in a device error word and reported by the
+ *    next attn_status() on that device.
+ *  - Values: Q, K, V and the mask must be finite, except that mask entries
+ *    may be -inf ("masked"). NaN or +inf inputs give undefined results (the
+ *    pages' row recurrence rejects them up front: "Explain FlashAttention and
+ *    why it is IO-aware", "Executable recurrence, with an empty-state
+ *    policy"). A query row whose every score is -inf (fully masked) returns
+ *    O = 0 and LSE = -inf, and contributes nothing to the gradients (same
+ *    section's empty-row policy).
+ *  - Empty problems (B, H or N equal to 0) are accepted and do nothing.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum attn_status_t {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = -1,     /* null pointer, negative size, bad flag or stride */
+    ATTN_ERR_UNSUPPORTED = -2, /* well-formed but not built: head dim, dtype pairing, size limit */
+    ATTN_ERR_ALIGN = -3,       /* a base pointer or byte stride is not a multiple of 16 */
+    ATTN_ERR_CUDA = -4,        /* a CUDA runtime or driver call failed */
+    ATTN_ERR_TIMEOUT = -5,     /* a kernel's bounded wait ran out (reported by attn_status) */
+    ATTN_ERR_WORKSPACE = -6    /* backward workspace missing or smaller than required */
+} attn_status_t;
+
+typedef enum attn_dtype_t {
+    ATTN_BF16 = 0, /* bfloat16 storage, fp32 accumulation (tcgen05 tensor cores) */
+    ATTN_F32 = 1   /* float32 storage and arithmetic (CUDA cores; forward only)   */
+} attn_dtype_t;
+
+/*
+ * Forward problem. O = softmax(scale * Q K^T + mask, causal) V and
+ * LSE = log(sum_j exp(s_ij)) over the scaled, masked scores of each row
+ * ("Explain FlashAttention and why it is IO-aware", "Keep only the state
+ * needed for the final weighted average").
+ */
+typedef struct attn_fwd_params {
+    int32_t B, H, N, d;      /* batch, heads, sequence length, head dim (64 or 128) */
+    int32_t dtype;           /* attn_dtype_t of Q, K, V, O (and the mask) */
+    int32_t causal;          /* 1: key j is masked for query i iff j > i (absolute
+                                positions, 0-based; same N for queries and keys) */
+    float scale;             /* softmax scale, > 0; 1/sqrt(d) is the usual choice */
+    int32_t reserved0;       /* must be 0 */
+    const void *q, *k, *v;   /* inputs, device memory */
+    void *o;                 /* output, device memory, same dtype as q */
+    float *lse;              /* output, device memory, float32 [B, H, N] */
+    int64_t q_stride[3];     /* element strides of (b, h, n) */
+    int64_t k_stride[3];
+    int64_t v_stride[3];
+    int64_t o_stride[3];
+    const void *mask;        /* optional additive mask, same dtype as q, logically
+                                [B, H, N, N] (query row, key column); NULL = none */
+    int64_t mask_stride[3];  /* element strides of (b, h, row); 0 broadcasts over
+                                that index; the key column is contiguous */
+} attn_fwd_params;
+
+/*
+ * Backward problem: dQ, dK, dV of sum(dO * O) for the forward described by
+ * `fwd`, whose o and lse (as written by attn_fwd) are READ here. Recomputes
+ * S and P tile by tile; no gradient flows to the mask. bf16 only.
+ */
+typedef struct attn_bwd_params {
+    attn_fwd_params fwd;
+    const void *dout;        /* dO, device memory, same dtype as q */
+    int64_t do_stride[3];
+    void *dq, *dk, *dv;      /* outputs, device memory, same dtype as q */
+    int64_t dq_stride[3];
+    int64_t dk_stride[3];
+    int64_t dv_stride[3];
+    void *workspace;         /* device memory, >= attn_bwd_workspace_size(&fwd)
+                                bytes, 256-byte aligned; contents need not be
+                                initialised and are scratch after the call */
+    size_t workspace_bytes;
+} attn_bwd_params;
+
+/* Forward pass (both dtypes). */
+ATTN_API attn_status_t attn_fwd(const attn_fwd_params *p, void *stream);
+
+/* Bytes of workspace attn_bwd needs for this problem (0 for an empty one):
+ * per (b, h) and 128-row query tile 1 KiB of fp32 row statistics
+ * (-LSE * log2(e) and D = rowsum(dO * O), padded to whole tiles), then the
+ * fp32 dQ accumulator [B, H, N, d]. */
+ATTN_API size_t attn_bwd_workspace_size(const attn_fwd_params *p);
+
+/* Backward pass: D pre-pass, recompute-and-accumulate kernel, dQ finalize. */
+ATTN_API attn_status_t attn_bwd(const attn_bwd_params *p, void *stream);
+
+/* Synchronizes `stream`, then reports (and clears) the current device's
+ * error word: ATTN_ERR_TIMEOUT if a kernel gave up on a bounded wait since
+ * the last call, ATTN_ERR_CUDA for an asynchronous CUDA error, else ATTN_OK. */
+ATTN_API attn_status_t attn_status(void *stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+ATTN_API const char *attn_last_error(void);
+
+/* Upper bound, in nanoseconds, on any single in-kernel wait (mbarrier or
+ * pipeline slot) before the kernel records ATTN_ERR_TIMEOUT and returns.
+ * Default 2e9 (2 s); values below 1e6 are raised to 1e6. Process-wide. */
+ATTN_API void attn_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook for failure detection: when > 0, the next forward launches on
+ * this host thread have their load warp stop after this many key/value
+ * tiles, so the consumers' bounded waits run out and report
+ * ATTN_ERR_TIMEOUT. 0 (the default) disables it. */
+ATTN_API void attn_debug_set_producer_stall(int32_t kv_tiles);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+ATTN_API int32_t attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

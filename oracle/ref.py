@@ -42,6 +42,13 @@ nothing. D is computed both ways and the two must agree to fp64 rounding.
 Inputs may be any float dtype (bf16 tensors are converted by the caller to
 fp64 exactly); everything is computed in fp64.
 
+Stored output. The backward consumes the O that the forward stored, and the
+library stores O in the dtype of Q. `attention_backward(..., o_storage=
+"bf16")` therefore also models that storage: the oracle rounds its own fp64 O
+to fp32 and then to bf16 (round to nearest even, as the kernels do from their
+fp32 accumulators) and takes D = rowsum(dO * O_stored) from it. Nothing else
+changes; with o_storage=None the result is the pure mathematical gradient.
+
 Parity pins: every function here is pinned by tests/test_oracle.py against
 the pages' worked numbers, closed forms, invariants, a scalar brute force,
 torch's fp64 scaled_dot_product_attention on the masked/causal special cases
@@ -58,6 +65,17 @@ CHUNK = 256
 
 def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
+
+
+def round_bf16(x) -> np.ndarray:
+    """fp64 -> fp32 -> bf16 (round to nearest, ties to even), returned as fp64."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    finite = np.isfinite(f)
+    out = np.where(finite, r, u & 0xFFFF0000).astype(np.uint32)
+    return out.view(np.float32).astype(np.float64)
 
 
 def _mask_for_head(mask: Optional[np.ndarray], b: int, h: int) -> Optional[np.ndarray]:
@@ -132,13 +150,15 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, mask=None):
 
 def backward_head(qh, kh, vh, doh, scale: float, causal: bool = False, maskh=None,
                   q_rows: Optional[Sequence[int]] = None,
-                  k_rows: Optional[Sequence[int]] = None):
+                  k_rows: Optional[Sequence[int]] = None, o_storage: Optional[str] = None):
     """Gradients of one head, by the closed form in the module docstring.
 
     Returns (dq[q_rows], dk[k_rows], dv[k_rows], D, D_from_o) where D and
-    D_from_o cover every query row. dK and dV of a key need every query row,
-    so the whole head is always swept; `q_rows` / `k_rows` only select which
-    gradient rows are returned (None = all).
+    D_from_o cover every query row. With o_storage="bf16", D is taken from
+    the bf16-rounded O (the stored output) instead of from P and dP.
+    dK and dV of a key need every query row, so the whole head is always
+    swept; `q_rows` / `k_rows` only select which gradient rows are returned
+    (None = all).
     """
     qh, kh, vh, doh = _f64(qh), _f64(kh), _f64(vh), _f64(doh)
     maskh = None if maskh is None else _f64(maskh)
@@ -157,9 +177,14 @@ def backward_head(qh, kh, vh, doh, scale: float, causal: bool = False, maskh=Non
         p, _ = row_softmax(head_scores(qh, kh, r, scale, causal, maskh))
         o_rows = p @ vh
         dp = doh[r] @ vh.T
-        d_rows = (p * dp).sum(axis=1)
-        D[r] = d_rows
         D_o[r] = (doh[r] * o_rows).sum(axis=1)
+        if o_storage == "bf16":
+            d_rows = (doh[r] * round_bf16(o_rows)).sum(axis=1)
+        elif o_storage is None:
+            d_rows = (p * dp).sum(axis=1)
+        else:
+            raise ValueError(f"unknown o_storage {o_storage!r}")
+        D[r] = d_rows
         ds = p * (dp - d_rows[:, None])
         want = q_pos[r] >= 0
         if want.any():
@@ -169,8 +194,10 @@ def backward_head(qh, kh, vh, doh, scale: float, causal: bool = False, maskh=Non
     return dq, dk, dv, D, D_o
 
 
-def attention_backward(q, k, v, do, scale: float, causal: bool = False, mask=None):
-    """dQ, dK, dV [B,H,N,d] and D [B,H,N] in fp64 (D checked both ways)."""
+def attention_backward(q, k, v, do, scale: float, causal: bool = False, mask=None,
+                       o_storage: Optional[str] = None):
+    """dQ, dK, dV [B,H,N,d] and D [B,H,N] in fp64 (D checked both ways when
+    o_storage is None)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     mask = None if mask is None else _f64(mask)
     B, H, N, d = q.shape
@@ -181,8 +208,9 @@ def attention_backward(q, k, v, do, scale: float, causal: bool = False, mask=Non
     for b in range(B):
         for h in range(H):
             dq[b, h], dk[b, h], dv[b, h], D[b, h], D_o = backward_head(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, _mask_for_head(mask, b, h))
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, _mask_for_head(mask, b, h),
+                o_storage=o_storage)
             scale_ref = max(1.0, float(np.abs(D[b, h]).max(initial=0.0)))
-            if not np.allclose(D[b, h], D_o, rtol=0.0, atol=1e-10 * scale_ref):
+            if o_storage is None and not np.allclose(D[b, h], D_o, rtol=0.0, atol=1e-10 * scale_ref):
                 raise AssertionError("D = rowsum(P * dP) and D = rowsum(dO * O) disagree")
     return dq, dk, dv, D

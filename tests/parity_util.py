@@ -1,0 +1,86 @@
+"""Comparison helpers shared by the GPU parity tests.
+
+Tolerances (written here once, used by every parity test):
+  * bf16 inputs, fp32 accumulation: max-abs error <= 2e-2 and relative-L2
+    error <= 5e-3 on O; gradients use the same two numbers, with the max-abs
+    bound taken relative to max(1, max |reference|) because a bf16 output of
+    magnitude M cannot be closer than its own rounding step (M * 2^-9).
+  * fp32 inputs: max-abs <= 1e-4 on O and LSE.
+  * LSE: max-abs <= 1e-3 on finite entries; -inf entries (fully masked rows)
+    must sit at exactly the same positions, and those rows of O must be 0.
+  * Gradients are held to the numbers above against the oracle's backward
+    given the stored output (O rounded to bf16 before D = rowsum(dO * O), as
+    the library stores it). Against the pure fp64 gradient, whose D uses the
+    unrounded O, the rounding of the stored O alone costs up to ~8e-3
+    relative-L2 when P is peaked or N is tiny (cancellation in dP - D), so
+    that comparison is bounded at GRAD_PURE_REL_L2.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+BF16_ATOL = 2e-2
+BF16_REL_L2 = 5e-3
+F32_ATOL = 1e-4
+LSE_ATOL = 1e-3
+GRAD_PURE_REL_L2 = 1.5e-2
+
+
+def to64(t) -> np.ndarray:
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def errors(got, want):
+    got, want = to64(got), to64(want)
+    diff = got - want
+    max_abs = float(np.max(np.abs(diff))) if diff.size else 0.0
+    denom = float(np.linalg.norm(want))
+    rel = float(np.linalg.norm(diff)) / denom if denom > 0 else float(np.linalg.norm(diff))
+    return max_abs, rel
+
+
+def assert_close_bf16(name, got, want, relative_max=False):
+    g, w = to64(got), to64(want)
+    max_abs, rel = errors(g, w)
+    bound = BF16_ATOL * (max(1.0, float(np.max(np.abs(w)))) if (relative_max and w.size) else 1.0)
+    assert max_abs <= bound and rel <= BF16_REL_L2, \
+        f"{name}: max-abs {max_abs:.3e} (bound {bound:.3e}), rel-L2 {rel:.3e} (bound {BF16_REL_L2:.1e})"
+    return max_abs, rel
+
+
+def assert_close_f32(name, got, want):
+    max_abs, rel = errors(got, want)
+    assert max_abs <= F32_ATOL, f"{name}: max-abs {max_abs:.3e} > {F32_ATOL:.0e}"
+    return max_abs, rel
+
+
+def assert_lse(got, want, atol=LSE_ATOL):
+    g, w = to64(got), to64(want)
+    fin_g, fin_w = np.isfinite(g), np.isfinite(w)
+    assert np.array_equal(fin_g, fin_w), "LSE: -inf rows differ"
+    assert np.all(np.isneginf(g[~fin_g])), "LSE: non-finite entries must be -inf"
+    if fin_w.any():
+        err = float(np.max(np.abs(g[fin_w] - w[fin_w])))
+        assert err <= atol, f"LSE: max-abs {err:.3e} > {atol:.0e}"
+        return err
+    return 0.0
+
+
+def assert_masked_rows_zero(o, lse_ref):
+    o = to64(o)
+    dead = np.isneginf(to64(lse_ref))
+    if dead.any():
+        assert np.all(o[dead] == 0.0), "fully masked rows of O must be exactly 0"
+
+
+def padded_mask(mask: torch.Tensor, device=None) -> torch.Tensor:
+    """The same values in storage whose rows are padded to a multiple of 8
+    elements (16 bytes), which the TMA-fed kernels require."""
+    n = mask.shape[-1]
+    npad = (n + 7) // 8 * 8
+    store = torch.zeros(*mask.shape[:-1], npad, dtype=mask.dtype, device=device or mask.device)
+    store[..., :n] = mask.to(store.device)
+    return store[..., :n]

@@ -500,3 +500,32 @@ def test_flops_formula():
     assert arith.attention_flops(1, 1, 8192, 128) == 4 * 8192**2 * 128
     assert arith.attention_flops(2, 32, 8192, 128, causal=True) == 2 * 32 * 8192**2 * 128 * 2
     assert arith.attention_flops(1, 1, 8, 2, causal=True, backward=True) == 2.5 * 4 * 64 * 2 / 2
+
+
+# ------------------------------------------------------ stored-output model
+def test_round_bf16_matches_torch():
+    r = _rng(31)
+    x = np.concatenate([r.standard_normal(20000) * 10.0 ** r.integers(-6, 6, 20000),
+                        [0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, np.inf, -np.inf]])
+    # exact ties in fp32 (low 16 bits == 0x8000) must round to even
+    ties = (np.arange(1, 200, dtype=np.uint32) << 16) | 0x3F800000 | 0x8000
+    x = np.concatenate([x, ties.view(np.float32).astype(np.float64)])
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    got = ref.round_bf16(x)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
+def test_backward_with_stored_bf16_output():
+    q, k, v, mask = _tiny_case(32, 1, 2, 40, 8, True, True)
+    do = _rng(33).standard_normal(q.shape)
+    dq, dk, dv, D = ref.attention_backward(q, k, v, do, 0.5, True, mask)
+    dq2, dk2, dv2, D2 = ref.attention_backward(q, k, v, do, 0.5, True, mask, o_storage="bf16")
+    o, _ = ref.attention_forward(q, k, v, 0.5, True, mask)
+    assert np.allclose(D2, (do * ref.round_bf16(o)).sum(-1), rtol=0, atol=1e-12)
+    assert np.array_equal(dv, dv2)  # dV does not involve D
+    # dQ and dK move by the D perturbation only: dS changes by -P * (D2 - D)
+    assert 0 < np.max(np.abs(dq2 - dq)) < 0.05 * np.max(np.abs(dq))
+    with pytest.raises(ValueError):
+        ref.attention_backward(q, k, v, do, 0.5, True, mask, o_storage="fp8")
