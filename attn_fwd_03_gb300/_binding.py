@@ -35,7 +35,8 @@ STATUS_NAMES = {
 
 # every symbol include/attn.h declares
 EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status", "attn_last_error",
-            "attn_set_wait_timeout_ns", "attn_debug_set_producer_stall", "attn_version")
+            "attn_set_wait_timeout_ns", "attn_debug_set_producer_stall", "attn_debug_set_bwd_events",
+            "attn_version")
 
 _i64x3 = ctypes.c_int64 * 3
 
@@ -86,6 +87,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_set_wait_timeout_ns.restype = None
     lib.attn_debug_set_producer_stall.argtypes = [ctypes.c_int32]
     lib.attn_debug_set_producer_stall.restype = None
+    lib.attn_debug_set_bwd_events.argtypes = [ctypes.c_void_p]
+    lib.attn_debug_set_bwd_events.restype = None
     lib.attn_version.argtypes = []
     lib.attn_version.restype = ctypes.c_int32
     return lib
@@ -205,6 +208,16 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def debug_set_producer_stall(kv_tiles: int) -> None:
     lib.attn_debug_set_producer_stall(int(kv_tiles))
+
+
+def debug_set_bwd_events(events=None) -> None:
+    """Time the three backward launches: `events` is four torch.cuda.Event
+    objects (already recorded once, so their handles exist) or None."""
+    if events is None:
+        lib.attn_debug_set_bwd_events(None)
+        return
+    handles = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+    lib.attn_debug_set_bwd_events(ctypes.cast(handles, ctypes.c_void_p))
 
 
 def version() -> int:

@@ -25,6 +25,13 @@ namespace {
 
 thread_local char t_last_error[512] = "";
 thread_local int32_t t_stall_after = 0;
+thread_local void* t_bwd_events[4] = {nullptr, nullptr, nullptr, nullptr};
+thread_local bool t_bwd_events_on = false;
+
+cudaError_t record_bwd_event(int i, cudaStream_t s) {
+    if (!t_bwd_events_on) return cudaSuccess;
+    return cudaEventRecord(static_cast<cudaEvent_t>(t_bwd_events[i]), s);
+}
 uint64_t g_timeout_ns = 2000000000ull;
 
 constexpr int kMaxDevices = 64;
@@ -248,12 +255,14 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
     const BwdWorkspace ws = bwd_workspace_split(*p);
     BwdMaps maps;
     if ((st = build_bwd_maps(*p, &maps)) != ATTN_OK) return st;
-    cudaError_t e = launch_bwd_prepass(*p, ws, lc.err, s);
+    cudaError_t e = record_bwd_event(0, s);
+    if (e == cudaSuccess) e = launch_bwd_prepass(*p, ws, lc.err, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd pre-pass launch");
-    e = launch_bwd_tc(*p, maps, ws, lc, s);
+    if ((e = record_bwd_event(1, s)) == cudaSuccess) e = launch_bwd_tc(*p, maps, ws, lc, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd main launch");
-    e = launch_bwd_dq_finalize(*p, ws, lc.err, s);
+    if ((e = record_bwd_event(2, s)) == cudaSuccess) e = launch_bwd_dq_finalize(*p, ws, lc.err, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dQ finalize launch");
+    if ((e = record_bwd_event(3, s)) != cudaSuccess) return cuda_fail(e, "attn_bwd event record");
     return ATTN_OK;
 }
 
@@ -282,6 +291,11 @@ const char* attn_last_error(void) { return t_last_error; }
 void attn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns = ns < 1000000ull ? 1000000ull : ns; }
 
 void attn_debug_set_producer_stall(int32_t kv_tiles) { t_stall_after = kv_tiles > 0 ? kv_tiles : 0; }
+
+void attn_debug_set_bwd_events(void* const events[4]) {
+    t_bwd_events_on = events != nullptr;
+    for (int i = 0; i < 4; ++i) t_bwd_events[i] = events ? events[i] : nullptr;
+}
 
 int32_t attn_version(void) { return 100; }
 

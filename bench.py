@@ -40,9 +40,9 @@ import workloads as W  # noqa: E402
 
 METRIC = "attention fwd/bwd TFLOP/s at 1 GB300 and % of dense bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# our kernels per step: forward 1, backward 3 (pre-pass, main, dQ finalize) in the
-# tensor-core path; the CUDA-core backward splits its main kernel in two
+# our kernels per step: forward 1, backward 3 (pre-pass, recompute kernel, dQ finalize)
 LAUNCHES_FWD = 1
+LAUNCHES_BWD = 3
 
 
 def load_peaks():
@@ -73,14 +73,19 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.first = 0
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.01)  # the sampler is running before the timed region starts
+            self.first = len(self.lines)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -100,7 +105,8 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in self.lines:
+        # samples taken after the timed region began (the last pre-region one included)
+        for line in self.lines[max(0, self.first - 1):]:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -174,7 +180,67 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------- cross-rank bookkeeping
+def reduce_max(values, dist=None, device=None):
+    """Element-wise max of per-rank timings over all ranks (identity for one rank)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(flops_per_rank_step: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica (weak scaling), timed
+    by the slowest rank."""
+    return flops_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ GPU arm
+def measure_workload(A, w, steps, warmup, dev, flush):
+    """fwd and bwd milliseconds of one workload (CUDA events on the launching
+    stream, L2 rewritten before every timed call)."""
+    import torch
+    inp = W.make_inputs(w)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    mask = inp["mask"].to(dev) if inp.get("mask") is not None else None
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    fwd = lambda: A.attn_fwd(q, k, v, scale=w.scale, causal=w.causal, mask=mask, out=o, lse=lse)  # noqa: E731
+    calls = [("fwd", fwd)]
+    if w.backward:
+        do = inp["do"].to(dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(max(A.bwd_workspace_size(q), 1), dtype=torch.uint8, device=dev)
+        bwd = lambda: A.attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask,  # noqa: E731
+                                 dq=dq, dk=dk, dv=dv, workspace=ws)
+        calls.append(("bwd", bwd))
+    for name, fn in calls:
+        for _ in range(warmup):
+            fwd()
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            flush.fill_(3)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        res[name] = sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+    if A.attn_status() != A.ATTN_OK:
+        raise RuntimeError(A.last_error())
+    out = {"shape": [w.B, w.H, w.N, w.d], "dtype": w.dtype, "causal": w.causal, "mask": w.mask}
+    f = W.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    out["fwd_ms"] = res["fwd"]
+    out["fwd_tflops"] = f / (res["fwd"] * 1e-3) / 1e12
+    if "bwd" in res:
+        out["bwd_ms"] = res["bwd"]
+        out["bwd_tflops"] = 2.5 * f / (res["bwd"] * 1e-3) / 1e12
+    return out
+
 def run_ours(args, w, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -184,19 +250,26 @@ def run_ours(args, w, rank, world, local_rank):
 
     peaks, peak_kind = load_peaks()
     inp = W.make_inputs(w)
-    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    do = inp["do"].to(dev) if w.backward else None
     mask = inp["mask"].to(dev) if inp.get("mask") is not None else None
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(max(A.bwd_workspace_size(q), 1), dtype=torch.uint8, device=dev)
+    dq = dk = dv = ws = None
+    if w.backward:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(max(A.bwd_workspace_size(q), 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    def bwd():
+        if w.backward:
+            A.attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask, dq=dq, dk=dk, dv=dv,
+                       workspace=ws)
+
     def step():
         A.attn_fwd(q, k, v, scale=w.scale, causal=w.causal, mask=mask, out=o, lse=lse)
-        A.attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask, dq=dq, dk=dk, dv=dv,
-                   workspace=ws)
+        bwd()
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -206,6 +279,12 @@ def run_ours(args, w, rank, world, local_rank):
         raise RuntimeError(A.last_error())
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # events the library records between its three backward launches
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for row in bev:
+        for e in row:
+            e.record(stream)  # creates the underlying CUDA event
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -215,9 +294,11 @@ def run_ours(args, w, rank, world, local_rank):
             ev[i][0].record(stream)
             A.attn_fwd(q, k, v, scale=w.scale, causal=w.causal, mask=mask, out=o, lse=lse)
             ev[i][1].record(stream)
-            A.attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask, dq=dq, dk=dk, dv=dv,
-                       workspace=ws)
+            if w.backward:
+                A.debug_set_bwd_events(bev[i])
+            bwd()
             ev[i][2].record(stream)
+        A.debug_set_bwd_events(None)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -228,36 +309,66 @@ def run_ours(args, w, rank, world, local_rank):
     ms = sum(f + b for f, b in zip(fwd_ms, bwd_ms)) / args.steps
     ms_fwd = sum(fwd_ms) / args.steps
     ms_bwd = sum(bwd_ms) / args.steps
-    if world > 1:
-        t = torch.tensor([ms, ms_fwd, ms_bwd], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_fwd, ms_bwd = t.tolist()
+    ms_main = ms_pre = ms_fin = 0.0
+    if w.backward:
+        ms_pre = sum(bev[i][0].elapsed_time(bev[i][1]) for i in range(args.steps)) / args.steps
+        ms_main = sum(bev[i][1].elapsed_time(bev[i][2]) for i in range(args.steps)) / args.steps
+        ms_fin = sum(bev[i][2].elapsed_time(bev[i][3]) for i in range(args.steps)) / args.steps
+    ms, ms_fwd, ms_bwd, ms_pre, ms_main, ms_fin = reduce_max([ms, ms_fwd, ms_bwd, ms_pre, ms_main, ms_fin],
+                                                             dist if world > 1 else None, dev)
 
     f_step = step_flops(w)
     f_fwd = step_flops(w, backward=False)
-    value = f_step * world / (ms * 1e-3) / 1e12
+    value = job_throughput(f_step, world, ms)
     peak = peaks["bf16_tflops"]
     fwd_tflops = f_fwd / (ms_fwd * 1e-3) / 1e12
-    bwd_tflops = (f_step - f_fwd) / (ms_bwd * 1e-3) / 1e12
+    bwd_tflops = (f_step - f_fwd) / (ms_bwd * 1e-3) / 1e12 if w.backward else None
+
+    # ---- per-kernel rooflines; the dominant kernel (most time per step) is reported as "roofline"
+    peak_src = f"{peak_kind} bf16_tflops (burst: kernels timed inside a step of a few ms)"
+    kernels = {"fwd_tc_kernel": {"ms": ms_fwd, "bound": "tensor", "achieved": fwd_tflops, "peak": peak,
+                                 "unit": "TFLOP/s", "frac": fwd_tflops / peak}}
+    if w.backward:
+        main_tflops = (f_step - f_fwd) / (ms_main * 1e-3) / 1e12
+        kernels["bwd_tc_kernel"] = {"ms": ms_main, "bound": "tensor", "achieved": main_tflops, "peak": peak,
+                                    "unit": "TFLOP/s", "frac": main_tflops / peak}
+        rows = w.B * w.H * w.N
+        pre_bytes = rows * w.d * 2 * 2 + rows * w.d * 4 + rows * 2 * 4 + rows * 4
+        fin_bytes = rows * w.d * 4 + rows * w.d * 2
+        hbm = peaks["hbm_gbs"]
+        for name, ms_k, nbytes in (("bwd_prepass_kernel", ms_pre, pre_bytes),
+                                   ("bwd_dq_finalize_kernel", ms_fin, fin_bytes)):
+            gbs = nbytes / (ms_k * 1e-3) / 1e9 if ms_k > 0 else None
+            kernels[name] = {"ms": ms_k, "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                             "frac": gbs / hbm if gbs else None}
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    roof = dict(kernels[dom])
+    roof.pop("ms")
+    roof.update({"kernel": dom, "traffic": None, "peak_source": peak_src,
+                 "note": "achieved = algorithmic FLOPs per launch / CUDA-event launch duration"})
 
     # ---- end to end through the public API with pinned host buffers
-    h_in = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
-    h_out = {"o": torch.empty_like(inp["q"]).pin_memory(), "lse": torch.empty(q.shape[:3]).pin_memory(),
-             "dq": torch.empty_like(inp["q"]).pin_memory(), "dk": torch.empty_like(inp["k"]).pin_memory(),
-             "dv": torch.empty_like(inp["v"]).pin_memory()}
+    in_names = ("q", "k", "v", "do") if w.backward else ("q", "k", "v")
+    h_in = {n: inp[n].pin_memory() for n in in_names}
+    dev_in = {"q": q, "k": k, "v": v, "do": do}
+    h_out = {"o": torch.empty_like(inp["q"]).pin_memory(), "lse": torch.empty(q.shape[:3]).pin_memory()}
+    dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    if w.backward:
+        for n, t in (("dq", inp["q"]), ("dk", inp["k"]), ("dv", inp["v"])):
+            h_out[n] = torch.empty_like(t).pin_memory()
     h_mask = inp["mask"].pin_memory() if inp.get("mask") is not None else None
     h2d = sum(t.numel() * t.element_size() for t in h_in.values()) + \
         (h_mask.numel() * h_mask.element_size() if h_mask is not None else 0)
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
     def e2e_step():
-        for n, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
-            dst.copy_(h_in[n], non_blocking=True)
+        for n in in_names:
+            dev_in[n].copy_(h_in[n], non_blocking=True)
         if h_mask is not None:
             mask.copy_(h_mask, non_blocking=True)
         step()
-        for n, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            h_out[n].copy_(src, non_blocking=True)
+        for n in h_out:
+            h_out[n].copy_(dev_out[n], non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -269,33 +380,39 @@ def run_ours(args, w, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
-    e2e_value = f_step * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = reduce_max([e2e_ms], dist if world > 1 else None, dev)[0]
+    e2e_value = job_throughput(f_step, world, e2e_ms)
 
     if rank != 0:
         return
-    launches_bwd = 4 if getattr(A, "BWD_LAUNCHES", None) is None else A.BWD_LAUNCHES
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**w.describe(), "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "256 MiB buffer rewritten before every timed step (inputs fit in L2)",
-                   "step": "attn_fwd + attn_bwd"},
+                   "step": "attn_fwd + attn_bwd" if w.backward else "attn_fwd"},
         "pct_of_peak": 100.0 * value / world / peak,
         "fwd": {"ms": ms_fwd, "tflops": fwd_tflops, "pct_of_peak": 100.0 * fwd_tflops / peak},
-        "bwd": {"ms": ms_bwd, "tflops": bwd_tflops, "pct_of_peak": 100.0 * bwd_tflops / peak},
-        "roofline": {"bound": "tensor", "kernel": "forward (one launch per attn_fwd)", "achieved": fwd_tflops,
-                     "peak": peak, "unit": "TFLOP/s", "frac": fwd_tflops / peak, "traffic": None,
-                     "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+        "bwd": ({"ms": ms_bwd, "tflops": bwd_tflops, "pct_of_peak": 100.0 * bwd_tflops / peak}
+                if w.backward else None),
+        "roofline": roof,
+        "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * (LAUNCHES_FWD + launches_bwd),
+        "gpu_launches": args.steps * (LAUNCHES_FWD + (LAUNCHES_BWD if w.backward else 0)),
         "clocks": clk.summary(),
     }
+    if world == 1 and not args.no_all:
+        peak = peaks["bf16_tflops"]
+        table = {}
+        for idx, wk in W.WORKLOADS.items():
+            r = measure_workload(A, wk, 10, 3, dev, flush)
+            for key in ("fwd", "bwd"):
+                if f"{key}_tflops" in r and wk.dtype == "bf16":
+                    r[f"{key}_pct_of_peak"] = 100.0 * r[f"{key}_tflops"] / peak
+            table[wk.name] = r
+        line["workloads"] = table
     if world == 1 and not args.no_cpu_baseline:
         el, fl, heads = oracle_sample(w, args.cpu_budget)
         line["cpu_baseline"] = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
@@ -307,13 +424,14 @@ def run_ours(args, w, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2, choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-all", action="store_true", help="skip the per-workload forward/backward table")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -142,6 +142,15 @@ ATTN_API void attn_set_wait_timeout_ns(uint64_t ns);
  * ATTN_ERR_TIMEOUT. 0 (the default) disables it. */
 ATTN_API void attn_debug_set_producer_stall(int32_t kv_tiles);
 
+/* Profiling hook: while `events` is non-NULL, every attn_bwd call on this
+ * host thread records events[0] before its pre-pass kernel, events[1] after
+ * it, events[2] after the recompute kernel and events[3] after the dQ
+ * finalize, on the call's stream, so a caller can time each of the three
+ * launches with CUDA events. The four cudaEvent_t handles are passed as
+ * void* and stay owned by the caller; the array is copied. NULL turns the
+ * hook off. */
+ATTN_API void attn_debug_set_bwd_events(void *const events[4]);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 ATTN_API int32_t attn_version(void);
 

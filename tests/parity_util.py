@@ -8,12 +8,16 @@ Tolerances (written here once, used by every parity test):
   * fp32 inputs: max-abs <= 1e-4 on O and LSE.
   * LSE: max-abs <= 1e-3 on finite entries; -inf entries (fully masked rows)
     must sit at exactly the same positions, and those rows of O must be 0.
-  * Gradients are held to the numbers above against the oracle's backward
-    given the stored output (O rounded to bf16 before D = rowsum(dO * O), as
-    the library stores it). Against the pure fp64 gradient, whose D uses the
-    unrounded O, the rounding of the stored O alone costs up to ~8e-3
-    relative-L2 when P is peaked or N is tiny (cancellation in dP - D), so
-    that comparison is bounded at GRAD_PURE_REL_L2.
+  * Gradients. The backward computes D = rowsum(dO * O) from the O the forward
+    stored in bf16, as the method prescribes (the backward recomputes from
+    the stored output and statistics). Where dP - D cancels (tiny N, peaked
+    P) that storage rounding alone moves dQ and dK by more than 5e-3 of their
+    norm, so the bound is derived from it: against the pure fp64 gradient,
+        rel-L2  <= 5e-3 + 2 * delta,   max-abs <= 2e-2 * max(1, max|ref|) + 2 * delta_abs,
+    where delta / delta_abs are the relative-L2 / max-abs change the oracle
+    itself sees when it takes D from its own bf16-rounded O instead of the
+    exact one. Both come from the oracle alone; for non-degenerate shapes
+    delta is ~1e-3.
 """
 from __future__ import annotations
 
@@ -24,7 +28,6 @@ BF16_ATOL = 2e-2
 BF16_REL_L2 = 5e-3
 F32_ATOL = 1e-4
 LSE_ATOL = 1e-3
-GRAD_PURE_REL_L2 = 1.5e-2
 
 
 def to64(t) -> np.ndarray:
@@ -74,6 +77,18 @@ def assert_masked_rows_zero(o, lse_ref):
     dead = np.isneginf(to64(lse_ref))
     if dead.any():
         assert np.all(o[dead] == 0.0), "fully masked rows of O must be exactly 0"
+
+
+def assert_grad(name, got, pure, stored):
+    """Gradient check with the stored-output allowance described above."""
+    g, w, st = to64(got), to64(pure), to64(stored)
+    delta_abs, delta = errors(st, w)
+    max_abs, rel = errors(g, w)
+    bound_abs = BF16_ATOL * max(1.0, float(np.max(np.abs(w))) if w.size else 1.0) + 2 * delta_abs
+    bound_rel = BF16_REL_L2 + 2 * delta
+    assert max_abs <= bound_abs and rel <= bound_rel, \
+        f"{name}: max-abs {max_abs:.3e} (bound {bound_abs:.3e}), rel-L2 {rel:.3e} (bound {bound_rel:.3e})"
+    return max_abs, rel
 
 
 def padded_mask(mask: torch.Tensor, device=None) -> torch.Tensor:
