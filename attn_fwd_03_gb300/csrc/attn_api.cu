@@ -203,6 +203,47 @@ BwdWorkspace bwd_workspace_split(const attn_bwd_params& p) {
     return BwdWorkspace{reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + stats_bytes(p.fwd))};
 }
 
+// ---- helpers for entry points that supply their own workspace storage
+attn_status_t report_error(attn_status_t st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+attn_status_t bwd_check_inputs(const attn_bwd_params* p, bool* empty) {
+    if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
+    attn_status_t st = check_fwd(&p->fwd, empty);
+    if (st != ATTN_OK) return st;
+    if (p->fwd.dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 only");
+    if (*empty) return ATTN_OK;
+    if ((st = check_tensor("dout", p->dout, p->do_stride, 2, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("dq", p->dq, p->dq_stride, 2, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("dk", p->dk, p->dk_stride, 2, false)) != ATTN_OK) return st;
+    return check_tensor("dv", p->dv, p->dv_stride, 2, false);
+}
+
+BwdWorkspace bwd_workspace_at(void* base, const attn_fwd_params& f) {
+    char* b = static_cast<char*>(base);
+    return BwdWorkspace{reinterpret_cast<float*>(b), reinterpret_cast<float*>(b + stats_bytes(f))};
+}
+
+attn_status_t bwd_launch_with(const attn_bwd_params& p, const BwdWorkspace& ws, void* stream) {
+    LaunchCommon lc;
+    attn_status_t st = device_setup(&lc);
+    if (st != ATTN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    BwdMaps maps;
+    if ((st = build_bwd_maps(p, &maps)) != ATTN_OK) return st;
+    cudaError_t e = launch_bwd_prepass(p, ws, lc.err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward pre-pass launch");
+    if ((e = launch_bwd_tc(p, maps, ws, lc, s)) != cudaSuccess) return cuda_fail(e, "backward main launch");
+    if ((e = launch_bwd_dq_finalize(p, ws, lc.err, s)) != cudaSuccess)
+        return cuda_fail(e, "backward dQ finalize launch");
+    return ATTN_OK;
+}
+
 }  // namespace attn
 
 using namespace attn;

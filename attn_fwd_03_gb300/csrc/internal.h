@@ -43,6 +43,12 @@ struct BwdWorkspace {
 size_t bwd_workspace_bytes(const attn_fwd_params& p);
 BwdWorkspace bwd_workspace_split(const attn_bwd_params& p);
 
+// attn_api.cu — shared by entry points that supply their own workspace storage.
+attn_status_t report_error(attn_status_t st, const char* fmt, ...);
+attn_status_t bwd_check_inputs(const attn_bwd_params* p, bool* empty);  // all but the workspace
+BwdWorkspace bwd_workspace_at(void* base, const attn_fwd_params& f);
+attn_status_t bwd_launch_with(const attn_bwd_params& p, const BwdWorkspace& ws, void* stream);
+
 // attn_fwd_sm103.cu — tcgen05 forward (bf16).
 cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);
 

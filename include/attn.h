@@ -123,6 +123,26 @@ ATTN_API size_t attn_bwd_workspace_size(const attn_fwd_params *p);
 /* Backward pass: D pre-pass, recompute-and-accumulate kernel, dQ finalize. */
 ATTN_API attn_status_t attn_bwd(const attn_bwd_params *p, void *stream);
 
+/* The same backward pass without a caller workspace: the scratch (row
+ * statistics and the fp32 dQ accumulator) lives in a 40 MiB array the
+ * library keeps in device memory, so this call allocates nothing. It is for
+ * callers that cannot call cudaMalloc or their framework's allocator where
+ * they run the backward (inside an allocator callback, in a plug-in whose
+ * host owns all memory, under a fixed memory budget). The source pages have
+ * no counterpart; it is a convenience of this library.
+ *  - Inputs and outputs are passed exactly as for attn_bwd; p->workspace and
+ *    p->workspace_bytes are ignored.
+ *  - Problems whose attn_bwd_workspace_size() exceeds 40 MiB are rejected
+ *    with ATTN_ERR_WORKSPACE before anything is launched.
+ *  - Every GPU that loads the library holds the 40 MiB until the process
+ *    exits. The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - All calls share the one array: calls that overlap on the GPU (other
+ *    streams, other threads) race and give wrong gradients. Each call
+ *    re-initialises everything it reads, so results do not depend on
+ *    earlier calls. */
+ATTN_API attn_status_t attn_bwd_noalloc(const attn_bwd_params *p, void *stream);
+
 /* Synchronizes `stream`, then reports (and clears) the current device's
  * error word: ATTN_ERR_TIMEOUT if a kernel gave up on a bounded wait since
  * the last call, ATTN_ERR_CUDA for an asynchronous CUDA error, else ATTN_OK. */
