@@ -19,18 +19,23 @@
 // global memory with vector reductions (other key tiles add to the same rows).
 //
 // Warp roles (12 warps):
-//   warps 0-3   P^T / dS^T from the score tiles (thread = key row), then the
-//               dK / dV epilogue
-//   warps 4-7   dQ drain (thread = query row of the tile)
+//   warps 0-7   two warpgroups; warpgroup g builds P^T / dS^T for query
+//               columns [64 g, 64 g + 64) of each tile (thread = key row),
+//               then drains its half of the dQ tile's columns (thread = query
+//               row); at the end warpgroup 0 writes dV and warpgroup 1 dK
 //   warp  8     TMA producer: K and V once, then per query tile Q_i, dO_i, the
-//               mask tile and the tile's -LSE*log2(e) and D statistics (1 KB,
+//               mask tile and the tile's -LSE*log2(e) and -D statistics (1 KB,
 //               written tile-padded by the pre-pass)
 //   warp  9     TMEM allocator and MMA issuer
 //   warps 10-11 idle
 //
 // Tensor memory (512 columns, lane = key row for S^T/dP^T/dK/dV, query row for dQ):
-//   [0,128)    S^T fp32; P^T bf16 pairs in [0,64); dQ columns 0-63 in [64,128)
-//   [128,256)  dP^T fp32; dS^T bf16 pairs in [128,192); dQ columns 64-127 in [192,256)
+//   [0,128)    S^T fp32; P^T bf16 pairs in [0,32) and [64,96) (see packed_col);
+//              then dQ columns 0-63 in [64,128)
+//   [128,256)  dP^T fp32; dS^T bf16 pairs in [128,160) and [192,224);
+//              then dQ columns 64-127 in [192,256)
+// The dQ MMAs overwrite packed P^T / dS^T columns only after the dV / dK MMAs
+// that read them: tcgen05 MMAs issued by one thread execute in order.
 //   [256,256+D)      dV accumulator
 //   [256+D,256+2D)   dK accumulator
 #include <cuda_bf16.h>
@@ -74,7 +79,7 @@ struct BwdParamsDev {
     int causal;
     float c;      // scale * log2(e)
     float scale;
-    const float* stats;  // [B*H][nq][2][128]: -LSE*log2e, then D
+    const float* stats;  // [B*H][nq][2][128]: -LSE*log2e, then -D
     float* dq_acc;
     __nv_bfloat16 *dk, *dv;
     long long dk_sb, dk_sh, dk_sn, dv_sb, dv_sh, dv_sn;
@@ -99,6 +104,14 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
     return sdesc_sw128(tile + kk * (16 * 128), 128 * 128, 1024);
 }
+// TMEM column (relative to the S^T or dP^T region) of the bf16 pairs for
+// query chunk c (32 queries): each warpgroup packs its results into the
+// first half of the 64 fp32 columns it has itself already read, never into
+// columns the other warpgroup may still be reading.
+__host__ __device__ constexpr int packed_col(int c) { return 64 * (c >> 1) + 16 * (c & 1); }
+// ... and of the 16 queries of MMA k-step kk.
+__host__ __device__ constexpr int packed_col_k(int kk) { return packed_col(kk >> 1) + 8 * (kk & 1); }
+
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
     const uint32_t a = smem_u32(bar);
     const uint64_t t0 = globaltimer();
@@ -142,9 +155,9 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&bar.st_empty[s], 1);
         }
         mbar_init(&bar.s_full, 1);
-        mbar_init(&bar.ds_ready, 128);
+        mbar_init(&bar.ds_ready, 256);
         mbar_init(&bar.dq_full, 1);
-        mbar_init(&bar.dq_empty, 128);
+        mbar_init(&bar.dq_empty, 256);
         mbar_init(&bar.kv_done, 1);
         mbar_init(&bar.drain, 1);
         fence_mbar_init();
@@ -227,11 +240,11 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + 256, tmem + kk * 8, mnmajor_desc(sdO, kk), Cfg::kIdescKV,
+                    mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), Cfg::kIdescKV,
                            (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + 256 + D, tmem + 128 + kk * 8, mnmajor_desc(sQ, kk), Cfg::kIdescKV,
+                    mma_ts(tmem + 256 + D, tmem + 128 + packed_col_k(kk), mnmajor_desc(sQ, kk), Cfg::kIdescKV,
                            (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int half = 0; half < D / 64; ++half)
@@ -250,13 +263,20 @@ __global__ void __launch_bounds__(384, 1)
             drain_wait(&bar.drain, 0, p.timeout_ns);
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ------------------------------------------------ P^T, dS^T (thread = key row)
-        const int kr = warp * 32 + lane;
+    } else if (warp < 8) {
+        // ------------------------------------------------ P^T, dS^T, then the dQ drain
+        // Two warpgroups share each query tile: warpgroup g takes query columns
+        // [64 g, 64 g + 64) of P^T / dS^T (thread = key row), then drains its half
+        // of the dQ tile's columns (thread = query row).
+        const int g = warp >> 2;
+        const int kr = (warp & 3) * 32 + lane;
         const int kg = k0 + kr;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tRow = tmem + lane_off;
         uint8_t* ds_row = smem + Cfg::kDSOff + kr * 128;
+        constexpr int kDqCols = D / 2;                                      // dQ columns per warpgroup
+        const uint32_t tDq = tRow + (D == 128 ? 64 + 128 * g : 64 + 32 * g);  // their TMEM columns
+        const float2 c2 = make_float2(p.c, p.c);
         bool ok = true;
         for (int it = 0; it < n_it && ok; ++it) {
             const int q0 = (i_begin + it) * BQ;
@@ -267,14 +287,15 @@ __global__ void __launch_bounds__(384, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             const uint8_t* stage = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
-            const float* nlv = reinterpret_cast<const float*>(stage + Cfg::kVecOffInStage);
-            const float* ddv = nlv + 128;
+            const float* nlv = reinterpret_cast<const float*>(stage + Cfg::kVecOffInStage);  // -LSE*log2e
+            const float* ndv = nlv + 128;                                                   // -D
             tc_fence_after();
             const bool diag = p.causal && (q0 == k0);
             const bool key_ok = kg < p.N;
             const uint8_t* mt = stage + 2 * Cfg::kTileBytes;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * g + cc;  // 32-column chunk of the tile
                 uint32_t sv[32], pv[32];
                 tmem_ld32(tRow + 32 * c, sv);
                 tmem_ld32(tRow + 128 + 32 * c, pv);
@@ -282,27 +303,28 @@ __global__ void __launch_bounds__(384, 1)
                 uint32_t pk[16], dk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    float pp[2], dd2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int q = 32 * c + i + e;
-                        float x = __uint_as_float(sv[i + e]) * p.c + nlv[q];
-                        if (MASK) {
-                            const int kb = kr >> 6, kc = (kr & 63) >> 3;
-                            const __nv_bfloat16 mv = *reinterpret_cast<const __nv_bfloat16*>(
-                                mt + kb * 128 * 128 + q * 128 + ((kc ^ (q & 7)) << 4) + (kr & 7) * 2);
-                            x += __bfloat162float(mv) * kLog2e;
-                        }
-                        if (!key_ok || (diag && q < kr)) x = -INFINITY;
-                        const float pr = ex2(x);
-                        pp[e] = pr;
-                        dd2[e] = pr * (__uint_as_float(pv[i + e]) - ddv[q]);
+                    const int q = 32 * c + i;
+                    const float2 nl = *reinterpret_cast<const float2*>(nlv + q);
+                    const float2 nd = *reinterpret_cast<const float2*>(ndv + q);
+                    float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl);
+                    if (MASK) {
+                        const int kb = kr >> 6, kc = (kr & 63) >> 3;
+                        const float m0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                            mt + kb * 128 * 128 + q * 128 + ((kc ^ (q & 7)) << 4) + (kr & 7) * 2));
+                        const float m1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                            mt + kb * 128 * 128 + (q + 1) * 128 + ((kc ^ ((q + 1) & 7)) << 4) + (kr & 7) * 2));
+                        x = ffma2(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
                     }
-                    pk[i / 2] = pack_bf16(pp[0], pp[1]);
-                    dk[i / 2] = pack_bf16(dd2[0], dd2[1]);
+                    if (!key_ok || (diag && q < kr)) x.x = -INFINITY;
+                    if (!key_ok || (diag && q + 1 < kr)) x.y = -INFINITY;
+                    const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+                    const float2 ds =
+                        fmul2(pr, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd));
+                    pk[i / 2] = pack_bf16(pr.x, pr.y);
+                    dk[i / 2] = pack_bf16(ds.x, ds.y);
                 }
-                tmem_st16(tRow + 16 * c, pk);
-                tmem_st16(tRow + 128 + 16 * c, dk);
+                tmem_st16(tRow + packed_col(c), pk);
+                tmem_st16(tRow + 128 + packed_col(c), dk);
                 // dS row kr, queries 32c .. 32c+31 -> box (32c / 64), chunks ((32c % 64) / 8) .. +3
                 uint8_t* box = ds_row + ((32 * c) >> 6) * (128 * 128);
 #pragma unroll
@@ -316,63 +338,54 @@ __global__ void __launch_bounds__(384, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar.ds_ready);
-        }
-        // epilogue: dV and scale * dK rows of this key tile
-        if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            tc_fence_after();
-            __nv_bfloat16* dvr = p.dv + b * p.dv_sb + h * p.dv_sh + (long long)kg * p.dv_sn;
-            __nv_bfloat16* dkr = p.dk + b * p.dk_sb + h * p.dk_sh + (long long)kg * p.dk_sn;
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                __nv_bfloat16* dst_row = which == 0 ? dvr : dkr;
-                const float mul = which == 0 ? 1.f : p.scale;
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tRow + 256 + which * D + c0, v);
-                    tmem_wait_ld();
-                    if (kg < p.N) {
-                        uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(
-                                pack_bf16(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
-                                pack_bf16(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
-                                pack_bf16(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
-                                pack_bf16(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
-                    }
-                }
-            }
-        }
-    } else if (warp < 8) {
-        // ------------------------------------------------ dQ drain (thread = query row)
-        const int qr = (warp - 4) * 32 + lane;
-        const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-        bool ok = true;
-        for (int it = 0; it < n_it && ok; ++it) {
+
+            // dQ drain: this warpgroup's half of the columns of the dQ tile (thread = query row)
             ok = mbar_wait(&bar.dq_full, it & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint32_t v[D];
-            tmem_ld32_at<0>(tmem + lane_off + 64, v);
-            tmem_ld32_at<32>(tmem + lane_off + 96, v);
-            if constexpr (D == 128) {
-                tmem_ld32_at<64>(tmem + lane_off + 192, v);
-                tmem_ld32_at<96>(tmem + lane_off + 224, v);
-            }
+            uint32_t v[kDqCols];
+            tmem_ld32_at<0>(tDq, v);
+            if constexpr (kDqCols == 64) tmem_ld32_at<32>(tDq + 32, v);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&bar.dq_empty);
-            const int qg = (i_begin + it) * BQ + qr;
+            const int qg = q0 + kr;  // lane = query row of the dQ tile
             if (qg < p.N) {
-                float* dst = p.dq_acc + (((long long)b * p.H + h) * p.N + qg) * D;
+                float* dst = p.dq_acc + (((long long)b * p.H + h) * p.N + qg) * D + g * kDqCols;
 #pragma unroll
-                for (int c = 0; c < D; c += 4)
-                    red_add_v4(dst + c, __uint_as_float(v[c]) * p.scale, __uint_as_float(v[c + 1]) * p.scale,
-                               __uint_as_float(v[c + 2]) * p.scale, __uint_as_float(v[c + 3]) * p.scale);
+                for (int c = 0; c < kDqCols; c += 4) {
+                    const float2 a0 = fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                            make_float2(p.scale, p.scale));
+                    const float2 a1 = fmul2(make_float2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])),
+                                            make_float2(p.scale, p.scale));
+                    red_add_v4(dst + c, a0.x, a0.y, a1.x, a1.y);
+                }
+            }
+        }
+        // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of this key tile
+        if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            __nv_bfloat16* dst_row = g == 0 ? p.dv + b * p.dv_sb + h * p.dv_sh + (long long)kg * p.dv_sn
+                                            : p.dk + b * p.dk_sb + h * p.dk_sh + (long long)kg * p.dk_sn;
+            const float mul = g == 0 ? 1.f : p.scale;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tRow + 256 + g * D + c0, v);
+                tmem_wait_ld();
+                if (kg < p.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(
+                            pack_bf16(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                            pack_bf16(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
+                            pack_bf16(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
+                            pack_bf16(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+                }
             }
         }
     }

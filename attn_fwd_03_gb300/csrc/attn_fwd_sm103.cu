@@ -404,17 +404,16 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                         if (col >= lim) su[col] = __float_as_uint(-INFINITY);
                     cc = 1.f;
                 }
-                // tile max (in the log2 domain after multiplying by cc)
-                float mx0 = __uint_as_float(su[0]), mx1 = __uint_as_float(su[1]);
-                float mx2 = __uint_as_float(su[2]), mx3 = __uint_as_float(su[3]);
+                // tile max (in the log2 domain after multiplying by cc): 3-input max, two chains
+                float mxa = fmax3(__uint_as_float(su[0]), __uint_as_float(su[1]), __uint_as_float(su[2]));
+                float mxb = fmax3(__uint_as_float(su[3]), __uint_as_float(su[4]), __uint_as_float(su[5]));
 #pragma unroll
-                for (int col = 4; col < BN; col += 4) {
-                    mx0 = fmaxf(mx0, __uint_as_float(su[col]));
-                    mx1 = fmaxf(mx1, __uint_as_float(su[col + 1]));
-                    mx2 = fmaxf(mx2, __uint_as_float(su[col + 2]));
-                    mx3 = fmaxf(mx3, __uint_as_float(su[col + 3]));
+                for (int col = 6; col < BN - 2; col += 4) {
+                    mxa = fmax3(mxa, __uint_as_float(su[col]), __uint_as_float(su[col + 1]));
+                    mxb = fmax3(mxb, __uint_as_float(su[col + 2]), __uint_as_float(su[col + 3]));
                 }
-                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cc;
+                mxa = fmax3(mxa, __uint_as_float(su[BN - 2]), __uint_as_float(su[BN - 1]));
+                const float m_tile = fmaxf(mxa, mxb) * cc;
                 float m_new = m_ref;
                 if (m_tile > m_ref + kRescaleThreshold) m_new = m_tile;
                 const bool moved = m_new != m_ref;
@@ -427,27 +426,37 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                         tmem_ld32(tO + c0, ov);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 r = fmul2(make_float2(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])),
+                                                   make_float2(alpha, alpha));
+                            ov[i] = __float_as_uint(r.x);
+                            ov[i + 1] = __float_as_uint(r.y);
+                        }
                         tmem_st32(tO + c0, ov);
                     }
                 }
                 m_ref = m_new;
                 const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                float sum0 = 0.f, sum1 = 0.f;
+                // p = 2^(s * cc - m): one packed FMA per pair, two exp2, one packed add, one convert
+                const float2 cc2 = make_float2(cc, cc), nm2 = make_float2(neg_m, neg_m);
+                float2 suma = make_float2(0.f, 0.f), sumb = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int c0 = 0; c0 < BN; c0 += 32) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(su[c0 + 2 * i]), cc, neg_m));
-                        const float p1 = ex2(fmaf(__uint_as_float(su[c0 + 2 * i + 1]), cc, neg_m));
-                        sum0 += p0;
-                        sum1 += p1;
-                        pk[i] = pack_bf16(p0, p1);
+                        const float2 x = ffma2(
+                            make_float2(__uint_as_float(su[c0 + 2 * i]), __uint_as_float(su[c0 + 2 * i + 1])), cc2, nm2);
+                        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                        if (i & 1)
+                            sumb = fadd2(sumb, pp);
+                        else
+                            suma = fadd2(suma, pp);
+                        pk[i] = pack_bf16(pp.x, pp.y);
                     }
                     tmem_st16(tS + c0 / 2, pk);
                 }
-                l = l * alpha + (sum0 + sum1);
+                l = l * alpha + ((suma.x + suma.y) + (sumb.x + sumb.y));
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&bar.p_full[t]);

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(128) fwd_simt_kernel(SimtArgs a) {
 
 // ------------------------------------------------------------ bwd pre-pass
 // G = D/8 threads per row, 8 elements (16 B) each. Rows run over the padded
-// range [B*H][ceil(N/128)*128]. For a real row it writes D = <dO, O> and
+// range [B*H][ceil(N/128)*128]. For a real row it writes -D = -<dO, O> and
 // -LSE * log2(e) into the stats block and zeroes the row of the fp32 dQ
 // accumulator; a padding row gets (-inf, 0) so the backward kernel can copy
 // whole 128-row tiles of statistics without bounds checks.
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(256) bwd_prepass_kernel(SimtArgs a, float* sta
         if (n < a.N) {
             const float l = a.lse[bh * a.N + n];
             nl = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-            dd = sum;
+            dd = -sum;
         }
         float* tile = stats + (bh * (n_pad / 128) + n / 128) * 256;
         tile[n % 128] = nl;

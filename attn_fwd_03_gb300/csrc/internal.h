@@ -34,7 +34,7 @@ struct BwdMaps {
 // The two parts of the backward workspace.
 //  stats:  per (b, h) and 128-row query tile, 128 values of -LSE * log2(e)
 //          (-inf for fully masked rows and padding rows) followed by 128 values
-//          of D = rowsum(dO * O); fp32 [B*H][ceil(N/128)][2][128]
+//          of -D = -rowsum(dO * O); fp32 [B*H][ceil(N/128)][2][128]
 //  dq_acc: fp32 [B, H, N, d] dQ accumulator (already multiplied by the scale)
 struct BwdWorkspace {
     float* stats;
