@@ -396,13 +396,341 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
+
+// ============================================================================
+// d = 64: half-tile pipelined variant.
+//
+// At d = 64 tensor memory has room to overlap the phases the d = 128 kernel
+// runs one after another. Each 128-query tile is processed as two halves of
+// 64 queries; the scores of a half go into one of two TMEM buffers, so while
+// the warpgroups turn half u into P^T / dS^T, the tensor core already runs
+// S^T / dP^T of half u+1 and dV / dK of half u-1. dQ of a whole tile has its
+// own TMEM columns and the dS tile two shared-memory buffers, so the dQ drain
+// is off the critical path too.
+//
+// Tensor memory (512 columns):
+//   [128h, 128h+64)       S^T of the half in buffer h (fp32, 64 queries);
+//                         P^T bf16 pairs of warpgroup g's 32 queries at 128h + 32g
+//   [128h+64, 128h+128)   dP^T; dS^T pairs at 128h + 64 + 32g
+//   [256,320) dV   [320,384) dK   [384,448) dQ (query rows = lanes)
+// ============================================================================
+template <bool MASK>
+struct Bwd64Cfg {
+    static constexpr int D = 64;
+    static constexpr int kTileBytes = 128 * D * 2;  // 16 KB: Q, K, V or dO tile (one 64-column box)
+    static constexpr int kMaskBytes = BQ * BK * 2;
+    static constexpr int kStages = 2;
+    static constexpr int kVecOffInStage = 2 * kTileBytes + (MASK ? kMaskBytes : 0);
+    static constexpr int kStageBytes = kVecOffInStage + 1024;
+    static constexpr int kDSBytes = BQ * BK * 2;  // one dS tile (two 64-query boxes)
+    static constexpr int kKOff = 0;
+    static constexpr int kVOff = kTileBytes;
+    static constexpr int kDSOff = 2 * kTileBytes;  // two dS buffers
+    static constexpr int kStageOff = kDSOff + 2 * kDSBytes;
+    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kSmemBytes = kBarOff + 256;
+    static constexpr uint32_t kIdescS = idesc_bf16(BK, 64, false, false);  // S^T / dP^T of a half
+    static constexpr uint32_t kIdescKV = idesc_bf16(BK, D, false, true);   // dV, dK (A in TMEM)
+    static constexpr uint32_t kIdescQ = idesc_bf16(BQ, D, true, true);     // dQ (A = dS query-major)
+};
+
+struct __align__(8) Bwd64Barriers {
+    uint64_t kv_full;
+    uint64_t st_full[2], st_empty[2];
+    uint64_t s_full[2], ds_ready[2];  // per TMEM buffer
+    uint64_t dq_full, dq_empty, kv_done, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// TMEM column, within a buffer, of the bf16 pairs for MMA k-step kk (16 queries) of a half.
+__host__ __device__ constexpr int half_packed_col(int kk) { return 32 * (kk >> 1) + 8 * (kk & 1); }
+
+template <bool MASK>
+__global__ void __launch_bounds__(384, 1)
+    bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_mask, const BwdParamsDev p) {
+    using Cfg = Bwd64Cfg<MASK>;
+    constexpr int D = 64;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    Bwd64Barriers& bar = *reinterpret_cast<Bwd64Barriers*>(smem + Cfg::kBarOff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    WaitCtl wc{p.err, &bar.abort_flag, p.timeout_ns};
+
+    // work unit: key tile kt of (b, h); early key tiles first (they see the most query tiles)
+    const int bh = p.B * p.H;
+    const int kt = blockIdx.x / bh;
+    const int b = (blockIdx.x % bh) / p.H, h = blockIdx.x % p.H;
+    const int k0 = kt * BK;
+    const int nq_all = (p.N + BQ - 1) / BQ;
+    const int i_begin = p.causal ? kt : 0;
+    const int n_it = nq_all - i_begin;
+    const int n_half = 2 * n_it;
+
+    if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
+        if (threadIdx.x == 0) atomicExch(p.err, -7);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        bar.abort_flag = 0;
+        mbar_init(&bar.kv_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.st_full[i], 1);
+            mbar_init(&bar.st_empty[i], 1);
+            mbar_init(&bar.s_full[i], 1);
+            mbar_init(&bar.ds_ready[i], 256);
+        }
+        mbar_init(&bar.dq_full, 1);
+        mbar_init(&bar.dq_empty, 256);
+        mbar_init(&bar.kv_done, 1);
+        mbar_init(&bar.drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&bar.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bar.tmem_base;
+    const uint32_t sK = smem_u32(smem + Cfg::kKOff), sV = smem_u32(smem + Cfg::kVOff);
+
+    if (warp == 8) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(&bar.kv_full, 2 * Cfg::kTileBytes);
+            tma_load_4d(smem + Cfg::kKOff, &tm_k, &bar.kv_full, 0, k0, h, b);
+            tma_load_4d(smem + Cfg::kVOff, &tm_v, &bar.kv_full, 0, k0, h, b);
+            const int hm = p.mask_hb ? h : 0, bm = p.mask_bb ? b : 0;
+            bool ok = true;
+            int it = 0;
+            for (; it < n_it && ok; ++it) {
+                const int s = it % Cfg::kStages;
+                ok = mbar_wait(&bar.st_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
+                if (!ok) break;
+                const int q0 = (i_begin + it) * BQ;
+                uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+                mbar_arrive_expect_tx(&bar.st_full[s], Cfg::kStageBytes);
+                tma_load_4d(st, &tm_q, &bar.st_full[s], 0, q0, h, b);
+                tma_load_4d(st + Cfg::kTileBytes, &tm_do, &bar.st_full[s], 0, q0, h, b);
+                if (MASK)
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_4d(st + 2 * Cfg::kTileBytes + bx * 128 * 128, &tm_mask, &bar.st_full[s],
+                                    k0 + bx * 64, q0, hm, bm);
+                bulk_load(st + Cfg::kVecOffInStage,
+                          p.stats + ((long long)(b * p.H + h) * nq_all + (i_begin + it)) * 256, 1024,
+                          &bar.st_full[s]);
+            }
+            const int last = it < Cfg::kStages ? it : Cfg::kStages;
+            for (int i = it - last; i < it; ++i)
+                drain_wait(&bar.st_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
+            drain_wait(&bar.kv_full, 0, p.timeout_ns);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(&bar.kv_full, 0, wc);
+            tc_fence_after();
+            for (int u = 0; u <= n_half && ok; ++u) {
+                if (u < n_half) {
+                    // S^T and dP^T of half u into buffer u & 1 (its previous contents were
+                    // read by the dV / dK MMAs of half u-2, issued earlier)
+                    const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
+                    if (hf == 0) {
+                        ok = mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
+                    const uint32_t sdO = sQ + Cfg::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + 128 * hf, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS,
+                               kk > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + 128 * hf + 64, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(&bar.s_full[hf]);
+                }
+                if (u > 0) {
+                    // dV, dK of half v = u - 1, then dQ when v closes a tile
+                    const int v = u - 1, itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
+                    ok = mbar_wait(&bar.ds_ready[hv], (v >> 1) & 1, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
+                    const uint32_t sdO = sQ + Cfg::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(tmem + 256, tmem + 128 * hv + half_packed_col(kk), mnmajor_desc(sdO, kk),
+                               Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(tmem + 320, tmem + 128 * hv + 64 + half_packed_col(kk), mnmajor_desc(sQ, kk),
+                               Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
+                    if (hv == 1) {
+                        if (itv > 0) {  // the previous tile's dQ has been read out of TMEM
+                            ok = mbar_wait(&bar.dq_empty, (itv - 1) & 1, wc);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (itv & 1) * Cfg::kDSBytes);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
+                                   kk > 0 ? 1u : 0u);
+                        mma_commit(&bar.dq_full);
+                        mma_commit(&bar.st_empty[sv]);
+                    }
+                }
+            }
+            if (ok) mma_commit(&bar.kv_done);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mma_commit(&bar.drain);
+            drain_wait(&bar.drain, 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ------------------------------------------------ P^T, dS^T (thread = key row), dQ drain
+        const int g = warp >> 2;  // this warpgroup's 32 queries of each half
+        const int kr = (warp & 3) * 32 + lane;
+        const int kg = k0 + kr;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tRow = tmem + lane_off;
+        const float2 c2 = make_float2(p.c, p.c);
+        bool ok = true;
+        auto drain_dq = [&](int itd) {
+            ok = mbar_wait(&bar.dq_full, itd & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) return;
+            tc_fence_after();
+            uint32_t v[32];
+            tmem_ld32(tRow + 384 + 32 * g, v);  // dQ columns 32g .. 32g+31, lane = query row
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bar.dq_empty);
+            const int qg = (i_begin + itd) * BQ + kr;
+            if (qg < p.N) {
+                float* dst = p.dq_acc + (((long long)b * p.H + h) * p.N + qg) * D + 32 * g;
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    const float2 a0 = fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                            make_float2(p.scale, p.scale));
+                    const float2 a1 = fmul2(make_float2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])),
+                                            make_float2(p.scale, p.scale));
+                    red_add_v4(dst + c, a0.x, a0.y, a1.x, a1.y);
+                }
+            }
+        };
+        for (int u = 0; u < n_half && ok; ++u) {
+            const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
+            const int q0 = (i_begin + it) * BQ;
+            ok = mbar_wait(&bar.s_full[hf], (u >> 1) & 1, wc);
+            ok = ok && mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint8_t* stage = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+            const int ql0 = 64 * hf + 32 * g;  // first query (within the tile) of this warpgroup's chunk
+            const float* nlv = reinterpret_cast<const float*>(stage + Cfg::kVecOffInStage) + ql0;  // -LSE*log2e
+            const float* ndv = nlv + 128;                                                            // -D
+            const bool diag = p.causal && (q0 == k0);
+            const bool key_ok = kg < p.N;
+            const uint8_t* mt = stage + 2 * Cfg::kTileBytes;
+            uint32_t sv[32], pv[32];
+            tmem_ld32(tRow + 128 * hf + 32 * g, sv);
+            tmem_ld32(tRow + 128 * hf + 64 + 32 * g, pv);
+            tmem_wait_ld();
+            uint32_t pk[16], dk[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const int q = ql0 + i;
+                const float2 nl = *reinterpret_cast<const float2*>(nlv + i);
+                const float2 nd = *reinterpret_cast<const float2*>(ndv + i);
+                float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl);
+                if (MASK) {
+                    const int kb = kr >> 6, kc = (kr & 63) >> 3;
+                    const float m0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                        mt + kb * 128 * 128 + q * 128 + ((kc ^ (q & 7)) << 4) + (kr & 7) * 2));
+                    const float m1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                        mt + kb * 128 * 128 + (q + 1) * 128 + ((kc ^ ((q + 1) & 7)) << 4) + (kr & 7) * 2));
+                    x = ffma2(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
+                }
+                if (!key_ok || (diag && q < kr)) x.x = -INFINITY;
+                if (!key_ok || (diag && q + 1 < kr)) x.y = -INFINITY;
+                const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+                const float2 ds = fmul2(pr, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd));
+                pk[i / 2] = pack_bf16(pr.x, pr.y);
+                dk[i / 2] = pack_bf16(ds.x, ds.y);
+            }
+            // packed pairs go into the first 16 of the 32 columns this thread just read
+            tmem_st16(tRow + 128 * hf + 32 * g, pk);
+            tmem_st16(tRow + 128 * hf + 64 + 32 * g, dk);
+            // dS row kr, queries ql0 .. ql0+31 of tile buffer (it & 1): box hf, chunks 4g .. 4g+3
+            uint8_t* box = smem + Cfg::kDSOff + (it & 1) * Cfg::kDSBytes + hf * (128 * 128) + kr * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int ch = 4 * g + j;
+                *reinterpret_cast<uint4*>(box + ((ch ^ (kr & 7)) << 4)) =
+                    make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar.ds_ready[hf]);
+            // after the first half of tile it, read out the previous tile's dQ
+            if (hf == 0 && it > 0) drain_dq(it - 1);
+        }
+        if (ok) drain_dq(n_it - 1);
+        // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of this key tile
+        if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            tc_fence_after();
+            __nv_bfloat16* dst_row = g == 0 ? p.dv + b * p.dv_sb + h * p.dv_sh + (long long)kg * p.dv_sn
+                                            : p.dk + b * p.dk_sb + h * p.dk_sh + (long long)kg * p.dk_sn;
+            const float mul = g == 0 ? 1.f : p.scale;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tRow + 256 + g * D + c0, v);
+                tmem_wait_ld();
+                if (kg < p.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(
+                            pack_bf16(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                            pack_bf16(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
+                            pack_bf16(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
+                            pack_bf16(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
 template <int D, bool MASK>
 cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, const BwdWorkspace& ws,
                             const LaunchCommon& lc, cudaStream_t s) {
-    using Cfg = BwdCfg<D, MASK>;
-    static_assert(Cfg::kSmemBytes <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg::kSmemBytes);
+    constexpr int kSmem = D == 64 ? Bwd64Cfg<MASK>::kSmemBytes : BwdCfg<D, MASK>::kSmemBytes;
+    static_assert(kSmem <= 232448, "shared memory budget");
+    auto kernel = D == 64 ? bwd_tc64_kernel<MASK> : bwd_tc_kernel<D, MASK>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     const attn_fwd_params& f = prm.fwd;
     BwdParamsDev p{};
@@ -428,8 +756,7 @@ cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, con
     p.err = lc.err;
     p.timeout_ns = lc.timeout_ns;
     const unsigned grid = (unsigned)(p.n_ktiles * f.B * f.H);
-    bwd_tc_kernel<D, MASK><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(maps.q, maps.k, maps.v, maps.dout,
-                                                                        maps.mask, p);
+    kernel<<<grid, 384, kSmem, s>>>(maps.q, maps.k, maps.v, maps.dout, maps.mask, p);
     return cudaGetLastError();
 }
 
