@@ -154,6 +154,23 @@ attn_status_t encode_bf16_map(CUtensorMap* m, const char* name, const void* base
     return ATTN_OK;
 }
 
+// fp32 map over the dQ accumulator [B, H, N, d] (contiguous), 32-column x 128-row
+// boxes with the 128-byte swizzle, used by the TMA reductions of the backward.
+attn_status_t encode_dq_acc_map(const attn_fwd_params& p, float* dq_acc, CUtensorMap* m) {
+    attn_status_t st = get_encoder();
+    if (st != ATTN_OK) return st;
+    const uint64_t d = (uint64_t)p.d, N = (uint64_t)p.N;
+    cuuint64_t dims[4] = {d, N, (cuuint64_t)p.H, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {d * 4, N * d * 4, (cuuint64_t)p.H * N * d * 4};
+    cuuint32_t box[4] = {32, 128, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(dq accumulator) failed with %d", (int)r);
+    return ATTN_OK;
+}
+
 attn_status_t build_fwd_maps(const attn_fwd_params& p, FwdMaps* m) {
     attn_status_t st = get_encoder();
     if (st != ATTN_OK) return st;
@@ -224,6 +241,10 @@ attn_status_t bwd_check_inputs(const attn_bwd_params* p, bool* empty) {
     return check_tensor("dv", p->dv, p->dv_stride, 2, false);
 }
 
+attn_status_t build_dq_acc_map(const attn_fwd_params& p, float* dq_acc, CUtensorMap* m) {
+    return encode_dq_acc_map(p, dq_acc, m);
+}
+
 BwdWorkspace bwd_workspace_at(void* base, const attn_fwd_params& f) {
     char* b = static_cast<char*>(base);
     return BwdWorkspace{reinterpret_cast<float*>(b), reinterpret_cast<float*>(b + stats_bytes(f))};
@@ -236,6 +257,7 @@ attn_status_t bwd_launch_with(const attn_bwd_params& p, const BwdWorkspace& ws, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     BwdMaps maps;
     if ((st = build_bwd_maps(p, &maps)) != ATTN_OK) return st;
+    if ((st = encode_dq_acc_map(p.fwd, ws.dq_acc, &maps.dq_acc)) != ATTN_OK) return st;
     cudaError_t e = launch_bwd_prepass(p, ws, lc.err, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward pre-pass launch");
     if ((e = launch_bwd_tc(p, maps, ws, lc, s)) != cudaSuccess) return cuda_fail(e, "backward main launch");
@@ -296,6 +318,7 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
     const BwdWorkspace ws = bwd_workspace_split(*p);
     BwdMaps maps;
     if ((st = build_bwd_maps(*p, &maps)) != ATTN_OK) return st;
+    if ((st = encode_dq_acc_map(p->fwd, ws.dq_acc, &maps.dq_acc)) != ATTN_OK) return st;
     cudaError_t e = record_bwd_event(0, s);
     if (e == cudaSuccess) e = launch_bwd_prepass(*p, ws, lc.err, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd pre-pass launch");

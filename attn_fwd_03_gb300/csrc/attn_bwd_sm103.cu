@@ -127,7 +127,8 @@ template <int D, bool MASK>
 __global__ void __launch_bounds__(384, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_mask, const BwdParamsDev p) {
+                  const __grid_constant__ CUtensorMap tm_mask, const __grid_constant__ CUtensorMap tm_dq,
+                  const BwdParamsDev p) {
     using Cfg = BwdCfg<D, MASK>;
     extern __shared__ __align__(1024) uint8_t smem[];
     BwdBarriers& bar = *reinterpret_cast<BwdBarriers*>(smem + Cfg::kBarOff);
@@ -413,13 +414,17 @@ __global__ void __launch_bounds__(384, 1)
 //                         P^T bf16 pairs of warpgroup g's 32 queries at 128h + 32g
 //   [128h+64, 128h+128)   dP^T; dS^T pairs at 128h + 64 + 32g
 //   [256,320) dV   [320,384) dK   [384,448) dQ (query rows = lanes)
+//
+// Warps (16): 0-7 P^T / dS^T (two warpgroups, 32 queries of each half each),
+// 8 TMA producer, 9 MMA issuer, 10-11 idle, 12-15 dQ drain. The drain has its
+// own warpgroup so the P^T / dS^T warps move on to the next half at once.
 // ============================================================================
 template <bool MASK>
 struct Bwd64Cfg {
     static constexpr int D = 64;
     static constexpr int kTileBytes = 128 * D * 2;  // 16 KB: Q, K, V or dO tile (one 64-column box)
     static constexpr int kMaskBytes = BQ * BK * 2;
-    static constexpr int kStages = 2;
+    static constexpr int kStages = MASK ? 1 : 2;
     static constexpr int kVecOffInStage = 2 * kTileBytes + (MASK ? kMaskBytes : 0);
     static constexpr int kStageBytes = kVecOffInStage + 1024;
     static constexpr int kDSBytes = BQ * BK * 2;  // one dS tile (two 64-query boxes)
@@ -427,7 +432,8 @@ struct Bwd64Cfg {
     static constexpr int kVOff = kTileBytes;
     static constexpr int kDSOff = 2 * kTileBytes;  // two dS buffers
     static constexpr int kStageOff = kDSOff + 2 * kDSBytes;
-    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kStgOff = kStageOff + kStages * kStageBytes;  // dQ staging: 2 boxes of 32 fp32 x 128 rows
+    static constexpr int kBarOff = kStgOff + BQ * D * 4;
     static constexpr int kSmemBytes = kBarOff + 256;
     static constexpr uint32_t kIdescS = idesc_bf16(BK, 64, false, false);  // S^T / dP^T of a half
     static constexpr uint32_t kIdescKV = idesc_bf16(BK, D, false, true);   // dV, dK (A in TMEM)
@@ -439,6 +445,7 @@ struct __align__(8) Bwd64Barriers {
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full[2], ds_ready[2];  // per TMEM buffer
     uint64_t dq_full, dq_empty, kv_done, drain;
+    uint64_t dq_staged, dq_free;      // dQ staging in shared memory filled / free again
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -447,10 +454,11 @@ struct __align__(8) Bwd64Barriers {
 __host__ __device__ constexpr int half_packed_col(int kk) { return 32 * (kk >> 1) + 8 * (kk & 1); }
 
 template <bool MASK>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_mask, const BwdParamsDev p) {
+                    const __grid_constant__ CUtensorMap tm_mask, const __grid_constant__ CUtensorMap tm_dq,
+                    const BwdParamsDev p) {
     using Cfg = Bwd64Cfg<MASK>;
     constexpr int D = 64;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -482,9 +490,11 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&bar.ds_ready[i], 256);
         }
         mbar_init(&bar.dq_full, 1);
-        mbar_init(&bar.dq_empty, 256);
+        mbar_init(&bar.dq_empty, 128);
         mbar_init(&bar.kv_done, 1);
         mbar_init(&bar.drain, 1);
+        mbar_init(&bar.dq_staged, 128);
+        mbar_init(&bar.dq_free, 1);
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -537,59 +547,64 @@ __global__ void __launch_bounds__(384, 1)
         if (lane == 0) {
             bool ok = mbar_wait(&bar.kv_full, 0, wc);
             tc_fence_after();
-            for (int u = 0; u <= n_half && ok; ++u) {
-                if (u < n_half) {
-                    // S^T and dP^T of half u into buffer u & 1 (its previous contents were
-                    // read by the dV / dK MMAs of half u-2, issued earlier)
-                    const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
-                    if (hf == 0) {
-                        ok = mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
-                        if (!ok) break;
+            // S^T and dP^T of half u into buffer u & 1 (its previous contents were read by
+            // the dV / dK MMAs of half u-2, issued earlier)
+            auto issue_scores = [&](int u) {
+                const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
+                if (hf == 0) {
+                    ok = mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+                    if (!ok) return;
+                    tc_fence_after();
+                }
+                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
+                const uint32_t sdO = sQ + Cfg::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128 * hf, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128 * hf + 64, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
+                           kk > 0 ? 1u : 0u);
+                mma_commit(&bar.s_full[hf]);
+            };
+            // dV, dK of half v, then dQ when v closes a tile (which also releases its stage)
+            auto issue_grads = [&](int v) {
+                const int itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
+                ok = mbar_wait(&bar.ds_ready[hv], (v >> 1) & 1, wc);
+                if (!ok) return;
+                tc_fence_after();
+                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
+                const uint32_t sdO = sQ + Cfg::kTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tmem + 256, tmem + 128 * hv + half_packed_col(kk), mnmajor_desc(sdO, kk), Cfg::kIdescKV,
+                           (v > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tmem + 320, tmem + 128 * hv + 64 + half_packed_col(kk), mnmajor_desc(sQ, kk),
+                           Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
+                if (hv == 1) {
+                    if (itv > 0) {  // the previous tile's dQ has been read out of TMEM
+                        ok = mbar_wait(&bar.dq_empty, (itv - 1) & 1, wc);
+                        if (!ok) return;
                         tc_fence_after();
                     }
-                    const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
-                    const uint32_t sdO = sQ + Cfg::kTileBytes;
+                    const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (itv & 1) * Cfg::kDSBytes);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + 128 * hf, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS,
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
                                kk > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + 128 * hf + 64, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
-                               kk > 0 ? 1u : 0u);
-                    mma_commit(&bar.s_full[hf]);
+                    mma_commit(&bar.dq_full);
+                    mma_commit(&bar.st_empty[sv]);
                 }
-                if (u > 0) {
-                    // dV, dK of half v = u - 1, then dQ when v closes a tile
-                    const int v = u - 1, itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
-                    ok = mbar_wait(&bar.ds_ready[hv], (v >> 1) & 1, wc);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
-                    const uint32_t sdO = sQ + Cfg::kTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + 256, tmem + 128 * hv + half_packed_col(kk), mnmajor_desc(sdO, kk),
-                               Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + 320, tmem + 128 * hv + 64 + half_packed_col(kk), mnmajor_desc(sQ, kk),
-                               Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
-                    if (hv == 1) {
-                        if (itv > 0) {  // the previous tile's dQ has been read out of TMEM
-                            ok = mbar_wait(&bar.dq_empty, (itv - 1) & 1, wc);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (itv & 1) * Cfg::kDSBytes);
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
-                                   kk > 0 ? 1u : 0u);
-                        mma_commit(&bar.dq_full);
-                        mma_commit(&bar.st_empty[sv]);
-                    }
-                }
+            };
+            for (int u = 0; u <= n_half && ok; ++u) {
+                // With a single stage the next tile's operands can only arrive after the
+                // previous tile released the stage, so its gradient MMAs go first.
+                const bool grads_first = Cfg::kStages == 1 && (u & 1) == 0;
+                if (grads_first && u > 0) issue_grads(u - 1);
+                if (ok && u < n_half) issue_scores(u);
+                if (ok && !grads_first && u > 0) issue_grads(u - 1);
             }
             if (ok) mma_commit(&bar.kv_done);
         }
@@ -608,29 +623,6 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t tRow = tmem + lane_off;
         const float2 c2 = make_float2(p.c, p.c);
         bool ok = true;
-        auto drain_dq = [&](int itd) {
-            ok = mbar_wait(&bar.dq_full, itd & 1, wc);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) return;
-            tc_fence_after();
-            uint32_t v[32];
-            tmem_ld32(tRow + 384 + 32 * g, v);  // dQ columns 32g .. 32g+31, lane = query row
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bar.dq_empty);
-            const int qg = (i_begin + itd) * BQ + kr;
-            if (qg < p.N) {
-                float* dst = p.dq_acc + (((long long)b * p.H + h) * p.N + qg) * D + 32 * g;
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float2 a0 = fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
-                                            make_float2(p.scale, p.scale));
-                    const float2 a1 = fmul2(make_float2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])),
-                                            make_float2(p.scale, p.scale));
-                    red_add_v4(dst + c, a0.x, a0.y, a1.x, a1.y);
-                }
-            }
-        };
         for (int u = 0; u < n_half && ok; ++u) {
             const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
             const int q0 = (i_begin + it) * BQ;
@@ -687,10 +679,7 @@ __global__ void __launch_bounds__(384, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bar.ds_ready[hf]);
-            // after the first half of tile it, read out the previous tile's dQ
-            if (hf == 0 && it > 0) drain_dq(it - 1);
         }
-        if (ok) drain_dq(n_it - 1);
         // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of this key tile
         if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
         ok = __all_sync(0xffffffffu, ok);
@@ -716,6 +705,64 @@ __global__ void __launch_bounds__(384, 1)
                 }
             }
         }
+    }
+
+    else if (warp >= 12) {
+        // ------------------------------------------------ dQ drain (thread = query row of the tile)
+        // scale * dQ goes to shared memory in the 128-byte-swizzled layout of the
+        // accumulator's tensor map (box bx = columns 32 bx .. 32 bx + 31), and one
+        // thread adds both boxes into the fp32 accumulator with TMA reductions.
+        // Rows beyond N are clipped by the tensor map.
+        const int qr = (warp & 3) * 32 + lane;
+        const uint32_t tRow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        uint8_t* stg = smem + Cfg::kStgOff;
+        const bool issuer = threadIdx.x == 384;
+        if (issuer) prefetch_tmap(&tm_dq);
+        bool ok = true;
+        for (int it = 0; it < n_it && ok; ++it) {
+            ok = mbar_wait(&bar.dq_full, it & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[64];
+            tmem_ld32_at<0>(tRow + 384, v);
+            tmem_ld32_at<32>(tRow + 416, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bar.dq_empty);
+            if (it > 0) {  // the previous tile's reduction has finished reading the staging area
+                ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int col = 32 * bx + 4 * c;
+                    const float2 a0 = fmul2(make_float2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])),
+                                            make_float2(p.scale, p.scale));
+                    const float2 a1 = fmul2(make_float2(__uint_as_float(v[col + 2]), __uint_as_float(v[col + 3])),
+                                            make_float2(p.scale, p.scale));
+                    *reinterpret_cast<float4*>(stg + bx * (BQ * 128) + qr * 128 + ((c ^ (qr & 7)) << 4)) =
+                        make_float4(a0.x, a0.y, a1.x, a1.y);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bar.dq_staged);
+            if (issuer) {
+                ok = mbar_wait(&bar.dq_staged, it & 1, wc);
+                if (ok) {
+                    const int q0 = (i_begin + it) * BQ;
+                    tma_reduce_add_4d(&tm_dq, stg, 0, q0, h, b);
+                    tma_reduce_add_4d(&tm_dq, stg + BQ * 128, 32, q0, h, b);
+                    bulk_commit();
+                    bulk_wait_read0();
+                    mbar_arrive(&bar.dq_free);
+                }
+            }
+        }
+        if (issuer) bulk_wait0();  // reductions complete before the CTA exits
     }
 
     tc_fence_before();
@@ -756,7 +803,7 @@ cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, con
     p.err = lc.err;
     p.timeout_ns = lc.timeout_ns;
     const unsigned grid = (unsigned)(p.n_ktiles * f.B * f.H);
-    kernel<<<grid, 384, kSmem, s>>>(maps.q, maps.k, maps.v, maps.dout, maps.mask, p);
+    kernel<<<grid, D == 64 ? 512 : 384, kSmem, s>>>(maps.q, maps.k, maps.v, maps.dout, maps.mask, maps.dq_acc, p);
     return cudaGetLastError();
 }
 

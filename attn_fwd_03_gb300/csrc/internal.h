@@ -29,6 +29,7 @@ struct FwdMaps {
 // Tensor maps for the tcgen05 backward.
 struct BwdMaps {
     CUtensorMap q, k, v, dout, mask;
+    CUtensorMap dq_acc;  // fp32 view of the workspace's dQ accumulator (32 x 128 boxes, 128-byte swizzle)
 };
 
 // The two parts of the backward workspace.
@@ -48,6 +49,7 @@ attn_status_t report_error(attn_status_t st, const char* fmt, ...);
 attn_status_t bwd_check_inputs(const attn_bwd_params* p, bool* empty);  // all but the workspace
 BwdWorkspace bwd_workspace_at(void* base, const attn_fwd_params& f);
 attn_status_t bwd_launch_with(const attn_bwd_params& p, const BwdWorkspace& ws, void* stream);
+attn_status_t build_dq_acc_map(const attn_fwd_params& p, float* dq_acc, CUtensorMap* m);
 
 // attn_fwd_sm103.cu — tcgen05 forward (bf16).
 cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);
