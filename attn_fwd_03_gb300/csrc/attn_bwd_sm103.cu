@@ -176,7 +176,8 @@ __global__ void __launch_bounds__(384, 1)
 
     if (warp == 8) {
         // ------------------------------------------------ producer
-        if (lane == 0) {
+        // The whole warp walks the schedule and waits; one elected lane issues the copies.
+        if (elect_one()) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
@@ -186,15 +187,18 @@ __global__ void __launch_bounds__(384, 1)
                 tma_load_4d(smem + Cfg::kKOff + bx * 128 * 128, &tm_k, &bar.kv_full, bx * 64, k0, h, b);
                 tma_load_4d(smem + Cfg::kVOff + bx * 128 * 128, &tm_v, &bar.kv_full, bx * 64, k0, h, b);
             }
-            const int hm = p.mask_hb ? h : 0, bm = p.mask_bb ? b : 0;
-            bool ok = true;
-            int it = 0;
-            for (; it < n_it && ok; ++it) {
-                const int s = it % Cfg::kStages;
-                ok = mbar_wait(&bar.st_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
-                if (!ok) break;
-                const int q0 = (i_begin + it) * BQ;
-                uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+        }
+        __syncwarp();
+        const int hm = p.mask_hb ? h : 0, bm = p.mask_bb ? b : 0;
+        bool ok = true;
+        int it = 0;
+        for (; it < n_it && ok; ++it) {
+            const int s = it % Cfg::kStages;
+            ok = mbar_wait_warp(&bar.st_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
+            if (!ok) break;
+            const int q0 = (i_begin + it) * BQ;
+            uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&bar.st_full[s], Cfg::kStageBytes);
                 for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
                     tma_load_4d(st + bx * 128 * 128, &tm_q, &bar.st_full[s], bx * 64, q0, h, b);
@@ -208,6 +212,9 @@ __global__ void __launch_bounds__(384, 1)
                           p.stats + ((long long)(b * p.H + h) * nq_all + (i_begin + it)) * 256, 1024,
                           &bar.st_full[s]);
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             const int last = it < Cfg::kStages ? it : Cfg::kStages;
             for (int i = it - last; i < it; ++i)
                 drain_wait(&bar.st_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
@@ -215,20 +222,21 @@ __global__ void __launch_bounds__(384, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ok = mbar_wait(&bar.kv_full, 0, wc);
-            tc_fence_after();
-            for (int it = 0; it < n_it && ok; ++it) {
-                const int s = it % Cfg::kStages;
-                ok = mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+        // Converged warp; one elected lane (always the same one) issues MMAs and commits.
+        bool ok = mbar_wait_warp(&bar.kv_full, 0, wc);
+        tc_fence_after();
+        for (int it = 0; it < n_it && ok; ++it) {
+            const int s = it % Cfg::kStages;
+            ok = mbar_wait_warp(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+            if (!ok) break;
+            if (it > 0) {  // S^T / dP^T overwrite the previous dQ tile
+                ok = mbar_wait_warp(&bar.dq_empty, (it - 1) & 1, wc);
                 if (!ok) break;
-                if (it > 0) {  // S^T / dP^T overwrite the previous dQ tile
-                    ok = mbar_wait(&bar.dq_empty, (it - 1) & 1, wc);
-                    if (!ok) break;
-                }
-                tc_fence_after();
-                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes);
-                const uint32_t sdO = sQ + Cfg::kTileBytes;
+            }
+            tc_fence_after();
+            const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes);
+            const uint32_t sdO = sQ + Cfg::kTileBytes;
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 0, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
@@ -236,9 +244,12 @@ __global__ void __launch_bounds__(384, 1)
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 128, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
                 mma_commit(&bar.s_full);
-                ok = mbar_wait(&bar.ds_ready, it & 1, wc);
-                if (!ok) break;
-                tc_fence_after();
+            }
+            __syncwarp();
+            ok = mbar_wait_warp(&bar.ds_ready, it & 1, wc);
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
                     mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), Cfg::kIdescKV,
@@ -256,10 +267,10 @@ __global__ void __launch_bounds__(384, 1)
                 mma_commit(&bar.dq_full);
                 mma_commit(&bar.st_empty[s]);
             }
-            if (ok) mma_commit(&bar.kv_done);
+            __syncwarp();
         }
-        __syncwarp();
-        if (lane == 0) {
+        if (elect_one()) {
+            if (ok) mma_commit(&bar.kv_done);
             mma_commit(&bar.drain);
             drain_wait(&bar.drain, 0, p.timeout_ns);
         }
@@ -509,7 +520,8 @@ __global__ void __launch_bounds__(512, 1)
 
     if (warp == 8) {
         // ------------------------------------------------ producer
-        if (lane == 0) {
+        // The whole warp walks the schedule and waits; one elected lane issues the copies.
+        if (elect_one()) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
@@ -517,15 +529,18 @@ __global__ void __launch_bounds__(512, 1)
             mbar_arrive_expect_tx(&bar.kv_full, 2 * Cfg::kTileBytes);
             tma_load_4d(smem + Cfg::kKOff, &tm_k, &bar.kv_full, 0, k0, h, b);
             tma_load_4d(smem + Cfg::kVOff, &tm_v, &bar.kv_full, 0, k0, h, b);
-            const int hm = p.mask_hb ? h : 0, bm = p.mask_bb ? b : 0;
-            bool ok = true;
-            int it = 0;
-            for (; it < n_it && ok; ++it) {
-                const int s = it % Cfg::kStages;
-                ok = mbar_wait(&bar.st_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
-                if (!ok) break;
-                const int q0 = (i_begin + it) * BQ;
-                uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+        }
+        __syncwarp();
+        const int hm = p.mask_hb ? h : 0, bm = p.mask_bb ? b : 0;
+        bool ok = true;
+        int it = 0;
+        for (; it < n_it && ok; ++it) {
+            const int s = it % Cfg::kStages;
+            ok = mbar_wait_warp(&bar.st_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
+            if (!ok) break;
+            const int q0 = (i_begin + it) * BQ;
+            uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&bar.st_full[s], Cfg::kStageBytes);
                 tma_load_4d(st, &tm_q, &bar.st_full[s], 0, q0, h, b);
                 tma_load_4d(st + Cfg::kTileBytes, &tm_do, &bar.st_full[s], 0, q0, h, b);
@@ -537,6 +552,9 @@ __global__ void __launch_bounds__(512, 1)
                           p.stats + ((long long)(b * p.H + h) * nq_all + (i_begin + it)) * 256, 1024,
                           &bar.st_full[s]);
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             const int last = it < Cfg::kStages ? it : Cfg::kStages;
             for (int i = it - last; i < it; ++i)
                 drain_wait(&bar.st_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
@@ -544,20 +562,21 @@ __global__ void __launch_bounds__(512, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            bool ok = mbar_wait(&bar.kv_full, 0, wc);
-            tc_fence_after();
-            // S^T and dP^T of half u into buffer u & 1 (its previous contents were read by
-            // the dV / dK MMAs of half u-2, issued earlier)
-            auto issue_scores = [&](int u) {
-                const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
-                if (hf == 0) {
-                    ok = mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
-                    if (!ok) return;
-                    tc_fence_after();
-                }
-                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
-                const uint32_t sdO = sQ + Cfg::kTileBytes;
+        // Converged warp; one elected lane (always the same one) issues MMAs and commits.
+        bool ok = mbar_wait_warp(&bar.kv_full, 0, wc);
+        tc_fence_after();
+        // S^T and dP^T of half u into buffer u & 1 (its previous contents were read by
+        // the dV / dK MMAs of half u-2, issued earlier)
+        auto issue_scores = [&](int u) {
+            const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
+            if (hf == 0) {
+                ok = mbar_wait_warp(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+                if (!ok) return;
+                tc_fence_after();
+            }
+            const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
+            const uint32_t sdO = sQ + Cfg::kTileBytes;
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 128 * hf, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
@@ -566,15 +585,18 @@ __global__ void __launch_bounds__(512, 1)
                     mma_ss(tmem + 128 * hf + 64, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
                            kk > 0 ? 1u : 0u);
                 mma_commit(&bar.s_full[hf]);
-            };
-            // dV, dK of half v, then dQ when v closes a tile (which also releases its stage)
-            auto issue_grads = [&](int v) {
-                const int itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
-                ok = mbar_wait(&bar.ds_ready[hv], (v >> 1) & 1, wc);
-                if (!ok) return;
-                tc_fence_after();
-                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
-                const uint32_t sdO = sQ + Cfg::kTileBytes;
+            }
+            __syncwarp();
+        };
+        // dV, dK of half v, then dQ when v closes a tile (which also releases its stage)
+        auto issue_grads = [&](int v) {
+            const int itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
+            ok = mbar_wait_warp(&bar.ds_ready[hv], (v >> 1) & 1, wc);
+            if (!ok) return;
+            tc_fence_after();
+            const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
+            const uint32_t sdO = sQ + Cfg::kTileBytes;
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_ts(tmem + 256, tmem + 128 * hv + half_packed_col(kk), mnmajor_desc(sdO, kk), Cfg::kIdescKV,
@@ -583,13 +605,16 @@ __global__ void __launch_bounds__(512, 1)
                 for (int kk = 0; kk < 4; ++kk)
                     mma_ts(tmem + 320, tmem + 128 * hv + 64 + half_packed_col(kk), mnmajor_desc(sQ, kk),
                            Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
-                if (hv == 1) {
-                    if (itv > 0) {  // the previous tile's dQ has been read out of TMEM
-                        ok = mbar_wait(&bar.dq_empty, (itv - 1) & 1, wc);
-                        if (!ok) return;
-                        tc_fence_after();
-                    }
-                    const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (itv & 1) * Cfg::kDSBytes);
+            }
+            __syncwarp();
+            if (hv == 1) {
+                if (itv > 0) {  // the previous tile's dQ has been read out of TMEM
+                    ok = mbar_wait_warp(&bar.dq_empty, (itv - 1) & 1, wc);
+                    if (!ok) return;
+                    tc_fence_after();
+                }
+                const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (itv & 1) * Cfg::kDSBytes);
+                if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
@@ -597,19 +622,19 @@ __global__ void __launch_bounds__(512, 1)
                     mma_commit(&bar.dq_full);
                     mma_commit(&bar.st_empty[sv]);
                 }
-            };
-            for (int u = 0; u <= n_half && ok; ++u) {
-                // With a single stage the next tile's operands can only arrive after the
-                // previous tile released the stage, so its gradient MMAs go first.
-                const bool grads_first = Cfg::kStages == 1 && (u & 1) == 0;
-                if (grads_first && u > 0) issue_grads(u - 1);
-                if (ok && u < n_half) issue_scores(u);
-                if (ok && !grads_first && u > 0) issue_grads(u - 1);
+                __syncwarp();
             }
-            if (ok) mma_commit(&bar.kv_done);
+        };
+        for (int u = 0; u <= n_half && ok; ++u) {
+            // With a single stage the next tile's operands can only arrive after the
+            // previous tile released the stage, so its gradient MMAs go first.
+            const bool grads_first = Cfg::kStages == 1 && (u & 1) == 0;
+            if (grads_first && u > 0) issue_grads(u - 1);
+            if (ok && u < n_half) issue_scores(u);
+            if (ok && !grads_first && u > 0) issue_grads(u - 1);
         }
-        __syncwarp();
-        if (lane == 0) {
+        if (elect_one()) {
+            if (ok) mma_commit(&bar.kv_done);
             mma_commit(&bar.drain);
             drain_wait(&bar.drain, 0, p.timeout_ns);
         }

@@ -16,7 +16,9 @@
 //   warps 0-3  softmax for query tile 0 (one thread per query row)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q tiles, then K_j, V_j into a ring of stages
-//   warp  9    TMEM allocator and MMA issuer (one elected lane)
+//   warp  9    TMEM allocator and MMA issuer
+// The producer and MMA warps run their loops converged, waits included, and
+// one elected lane issues each batch of copies or MMAs.
 //   warp 10    TMA producer for the additive mask tiles (mask variant only)
 //   warp 11    idle
 // The launch gives every thread 168 registers (384 x 168 = 64512); the
@@ -199,42 +201,52 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
       regs_decrease<Cfg::kOtherRegs>();
       if (warp == 8) {
         // ------------------------------------------------ K/V producer
-        if (lane == 0) {
+        // The whole warp walks the schedule and waits; one elected lane issues the copies.
+        if (elect_one()) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            uint32_t it = 0, n_units = 0;
-            int tiles_issued = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++n_units) {
-                const Unit w = decode_unit(p, u);
-                ok = mbar_wait(&bar.q_empty, (n_units & 1) ^ 1, wc);
-                if (!ok) break;
-                const int nt = w.nkv[1] > 0 ? 2 : 1;
+        }
+        __syncwarp();
+        uint32_t it = 0, n_units = 0;
+        int tiles_issued = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++n_units) {
+            const Unit w = decode_unit(p, u);
+            ok = mbar_wait_warp(&bar.q_empty, (n_units & 1) ^ 1, wc);
+            if (!ok) break;
+            const int nt = w.nkv[1] > 0 ? 2 : 1;
+            if (elect_one()) {
                 mbar_arrive_expect_tx(&bar.q_full, nt * Cfg::kTileBytes);
                 for (int t = 0; t < nt; ++t)
                     for (int bx = 0; bx < Cfg::kBoxes; ++bx)
                         tma_load_4d(smem + Cfg::kQOff + t * Cfg::kTileBytes + bx * BM * 128, &tm_q, &bar.q_full,
                                     bx * 64, w.row0[t], w.h, w.b);
-                for (int j = 0; j < w.nkv_max && ok; ++j) {
-                    if (p.stall_after > 0 && tiles_issued >= p.stall_after) {
-                        ok = false;  // test hook: stop feeding the consumers
-                        break;
-                    }
-                    for (int kv = 0; kv < 2; ++kv, ++it) {
-                        const uint32_t s = it % Cfg::kStages;
-                        ok = mbar_wait(&bar.kv_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
-                        if (!ok) break;
+            }
+            __syncwarp();
+            for (int j = 0; j < w.nkv_max && ok; ++j) {
+                if (p.stall_after > 0 && tiles_issued >= p.stall_after) {
+                    ok = false;  // test hook: stop feeding the consumers
+                    break;
+                }
+                for (int kv = 0; kv < 2; ++kv, ++it) {
+                    const uint32_t s = it % Cfg::kStages;
+                    ok = mbar_wait_warp(&bar.kv_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
+                    if (!ok) break;
+                    if (elect_one()) {
                         mbar_arrive_expect_tx(&bar.kv_full[s], Cfg::kTileBytes);
                         uint8_t* dst = smem + Cfg::kKVOff + s * Cfg::kTileBytes;
                         for (int bx = 0; bx < Cfg::kBoxes; ++bx)
                             tma_load_4d(dst + bx * BN * 128, kv == 0 ? &tm_k : &tm_v, &bar.kv_full[s], bx * 64,
                                         j * BN, w.h, w.b);
                     }
-                    ++tiles_issued;
+                    __syncwarp();
                 }
+                ++tiles_issued;
             }
-            // drain: every copy issued must land before the CTA exits
+        }
+        // drain: every copy issued must land before the CTA exits
+        if (lane == 0) {
             const uint32_t last = it < (uint32_t)Cfg::kStages ? it : (uint32_t)Cfg::kStages;
             for (uint32_t i = it - last; i < it; ++i)
                 drain_wait(&bar.kv_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
@@ -268,67 +280,77 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t it = 0, n_units = 0, pcnt[2] = {0, 0}, ocnt[2] = {0, 0};
-            bool ok = true;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++n_units) {
-                const Unit w = decode_unit(p, u);
-                ok = mbar_wait(&bar.q_full, n_units & 1, wc);
-                if (!ok) break;
+        // The whole warp walks the schedule and waits; one elected lane (the same
+        // one every time: the warp is converged) issues the MMAs and their commits.
+        uint32_t it = 0, n_units = 0, pcnt[2] = {0, 0}, ocnt[2] = {0, 0};
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++n_units) {
+            const Unit w = decode_unit(p, u);
+            ok = mbar_wait_warp(&bar.q_full, n_units & 1, wc);
+            if (!ok) break;
+            tc_fence_after();
+            for (int j = 0; j <= w.nkv_max && ok; ++j) {
+                const uint32_t itK = it;  // ring slot of K_j; V_j follows it
+                const uint32_t sK = itK % Cfg::kStages, sV_prev = (itK + Cfg::kStages - 1) % Cfg::kStages;
+                if (j < w.nkv_max) {
+                    ok = mbar_wait_warp(&bar.kv_full[sK], (itK / Cfg::kStages) & 1, wc);
+                    if (!ok) break;
+                }
+                if (j > 0) {  // V_{j-1} lives in the slot before K_j
+                    ok = mbar_wait_warp(&bar.kv_full[sV_prev], ((itK - 1) / Cfg::kStages) & 1, wc);
+                    if (!ok) break;
+                }
                 tc_fence_after();
-                for (int j = 0; j <= w.nkv_max && ok; ++j) {
-                    const uint32_t itK = it;  // ring slot of K_j; V_j follows it
-                    const uint32_t sK = itK % Cfg::kStages, sV_prev = (itK + Cfg::kStages - 1) % Cfg::kStages;
-                    if (j < w.nkv_max) {
-                        ok = mbar_wait(&bar.kv_full[sK], (itK / Cfg::kStages) & 1, wc);
-                        if (!ok) break;
-                    }
-                    if (j > 0) {  // V_{j-1} lives in the slot before K_j
-                        ok = mbar_wait(&bar.kv_full[sV_prev], ((itK - 1) / Cfg::kStages) & 1, wc);
-                        if (!ok) break;
-                    }
-                    tc_fence_after();
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (w.nkv[t] == 0 || j > w.nkv[t]) continue;
-                        const uint32_t tS = tmem + t * BN, tO = tmem + 256 + t * D;
-                        if (j > 0) {
-                            // O_t += P_t^{j-1} V_{j-1}
-                            if (j == 1) {  // first PV of the unit overwrites O_t: epilogue must be done with it
-                                ok = mbar_wait(&bar.o_empty[t], (ocnt[t] & 1) ^ 1, wc);
-                                if (!ok) break;
-                            }
-                            ok = mbar_wait(&bar.p_full[t], pcnt[t] & 1, wc);
-                            if (!ok) break;
-                            ++pcnt[t];
-                            tc_fence_after();
-                            const uint32_t vt = sKV + sV_prev * Cfg::kTileBytes;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (!ok || w.nkv[t] == 0 || j > w.nkv[t]) continue;
+                    const uint32_t tS = tmem + t * BN, tO = tmem + 256 + t * D;
+                    if (j > 0) {
+                        // O_t += P_t^{j-1} V_{j-1}
+                        if (j == 1) {  // first PV of the unit overwrites O_t: epilogue must be done with it
+                            ok = mbar_wait_warp(&bar.o_empty[t], (ocnt[t] & 1) ^ 1, wc);
+                            if (!ok) continue;
+                        }
+                        ok = mbar_wait_warp(&bar.p_full[t], pcnt[t] & 1, wc);
+                        if (!ok) continue;
+                        ++pcnt[t];
+                        tc_fence_after();
+                        const uint32_t vt = sKV + sV_prev * Cfg::kTileBytes;
+                        if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < BN / 16; ++kk)
                                 mma_ts(tO, tS + kk * 8, vmajor_desc(vt, kk), Cfg::kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
                         }
-                        if (j < w.nkv[t]) {
-                            // S_t^j = Q_t K_j^T
-                            const uint32_t qt = sQ + t * Cfg::kTileBytes, kt = sKV + sK * Cfg::kTileBytes;
+                        __syncwarp();
+                    }
+                    if (j < w.nkv[t]) {
+                        // S_t^j = Q_t K_j^T
+                        const uint32_t qt = sQ + t * Cfg::kTileBytes, kt = sKV + sK * Cfg::kTileBytes;
+                        if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
                                 mma_ss(tS, kmajor_desc(qt, kk), kmajor_desc(kt, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
                             mma_commit(&bar.s_full[t]);
-                        } else {
-                            mma_commit(&bar.o_full[t]);  // last PV of this tile issued
-                            ++ocnt[t];
                         }
+                        __syncwarp();
+                    } else {
+                        if (elect_one()) mma_commit(&bar.o_full[t]);  // last PV of this tile issued
+                        __syncwarp();
+                        ++ocnt[t];
                     }
-                    if (!ok) break;
+                }
+                if (!ok) break;
+                if (elect_one()) {
                     if (j == w.nkv_max - 1) mma_commit(&bar.q_empty);  // last S of the unit issued
                     if (j < w.nkv_max) mma_commit(&bar.kv_empty[sK]);
                     if (j > 0) mma_commit(&bar.kv_empty[sV_prev]);
-                    if (j < w.nkv_max) it += 2;
                 }
+                __syncwarp();
+                if (j < w.nkv_max) it += 2;
             }
         }
-        __syncwarp();
         // every MMA this warp issued completes before TMEM is released
-        if (lane == 0) {
+        if (elect_one()) {
             mma_commit(&bar.drain);
             drain_wait(&bar.drain, 0, p.timeout_ns);
         }
