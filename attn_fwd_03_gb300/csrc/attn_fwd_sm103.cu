@@ -16,26 +16,33 @@
 //   warps 0-3  softmax for query tile 0 (one thread per query row)
 //   warps 4-7  softmax for query tile 1
 //   warp  8    TMA producer: Q tiles, then K_j, V_j into a ring of stages
-//   warp  9    TMEM allocator and MMA issuer
+//   warp  9    TMEM allocator; MMA issuer (d = 128: both tiles; d = 64: tile 0)
+//   warp 10    TMA producer for the additive mask tiles (mask variant only)
+//   warp 11    MMA issuer for tile 1 (d = 64), else idle
 // The producer and MMA warps run their loops converged, waits included, and
 // one elected lane issues each batch of copies or MMAs.
-//   warp 10    TMA producer for the additive mask tiles (mask variant only)
-//   warp 11    idle
 // The launch gives every thread 168 registers (384 x 168 = 64512); the
-// softmax warpgroups then raise theirs to 216 and the third warpgroup drops
-// to 72 (2 x 128 x 216 + 128 x 72 = 64512), so a thread can hold a whole
-// 128-column score row in registers.
+// softmax warpgroups then raise theirs (216 for d = 128, 208 for d = 64) and
+// the third warpgroup drops to the rest (72 or 88), so a thread can hold a
+// whole 128-column score row in registers.
 //
-// Tensor memory (512 columns x 128 lanes, lane = query row):
+// Tensor memory (512 columns x 128 lanes, lane = query row), d = 128:
 //   [0,128)        S_0 (fp32 scores of tile 0); P_0 (bf16 pairs) in its first 64 columns
 //   [128,256)      S_1 / P_1
-//   [256,256+D)    O_0 (fp32 accumulator)
-//   [256+D,256+2D) O_1
-//
+//   [256,384)      O_0 (fp32 accumulator)
+//   [384,512)      O_1
 // Per key tile j and query tile t the MMA warp issues O_t += P_t^{j-1} V_{j-1}
 // and then S_t^j = Q_t K_j^T; tcgen05 MMAs from one thread run in issue order,
 // so S_t^j overwriting P_t^{j-1} is safe, and the commit that signals S_t^j
 // also covers the previous PV, which lets the softmax warps rescale O_t.
+//
+// d = 64 ("split P"): S_0 [0,128), S_1 [128,256), O_0 [256,320), O_1 [320,384),
+// P_0 [384,448), P_1 [448,512). The softmax warps release S_t (s_free) as soon
+// as they have loaded it, so S_t^{j+1} is computed while they still work on
+// S_t^j; the PV product signals its own completion (pv_done), which the
+// softmax warps wait for before they rescale O_t or overwrite P_t. At d = 64
+// the matrix products are short next to the softmax, and this keeps the
+// softmax warps from waiting on them.
 //
 // Online softmax in the log2 domain ("Explain FlashAttention and why it is
 // IO-aware", "Keep only the state needed for the final weighted average";
@@ -71,10 +78,15 @@ struct FwdCfg {
     static constexpr int kBoxes = D / 64;                  // 64-column (128-byte) TMA boxes per row
     static constexpr int kTileBytes = BM * D * 2;          // one Q, K or V tile
     static constexpr int kStages = (D == 128) ? (MASK ? 3 : 4) : (MASK ? 6 : 8);
+    // d = 64: P gets its own TMEM columns and each query tile its own MMA issuer
+    static constexpr bool kSplit = D == 64;
+    static constexpr int kIssuers = kSplit ? 2 : 1;
     static constexpr int kMaskBytes = BM * BN * 2;
     static constexpr int kWarps = 12;
-    static constexpr int kSoftmaxRegs = 216;
-    static constexpr int kOtherRegs = 72;
+    // per-thread registers after the rebalance: 2 x 128 x softmax + 128 x other = 384 x 168
+    static constexpr int kSoftmaxRegs = D == 64 ? 208 : 216;
+    static constexpr int kOtherRegs = D == 64 ? 88 : 72;
+    static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= 384 * 168, "register split");
     static constexpr int kThreads = kWarps * 32;
     // shared memory layout (offsets from a 1024-aligned base)
     static constexpr int kQOff = 0;
@@ -104,8 +116,9 @@ struct __align__(8) Barriers {
     uint64_t q_full, q_empty;
     uint64_t kv_full[8], kv_empty[8];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    uint64_t s_free[2], pv_done[2];  // split-P layout only
     uint64_t m_full[2], m_empty[2];
-    uint64_t drain;
+    uint64_t drain[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -170,10 +183,10 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
     if (threadIdx.x == 0) {
         bar.abort_flag = 0;
         mbar_init(&bar.q_full, 1);
-        mbar_init(&bar.q_empty, 1);
+        mbar_init(&bar.q_empty, Cfg::kIssuers);
         for (int s = 0; s < Cfg::kStages; ++s) {
             mbar_init(&bar.kv_full[s], 1);
-            mbar_init(&bar.kv_empty[s], 1);
+            mbar_init(&bar.kv_empty[s], Cfg::kIssuers);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bar.s_full[t], 1);
@@ -182,8 +195,10 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
             mbar_init(&bar.o_empty[t], BM);
             mbar_init(&bar.m_full[t], 1);
             mbar_init(&bar.m_empty[t], BM);
+            mbar_init(&bar.s_free[t], BM);
+            mbar_init(&bar.pv_done[t], 1);
+            mbar_init(&bar.drain[t], 1);
         }
-        mbar_init(&bar.drain, 1);
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -278,6 +293,85 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
             for (int t = 0; t < 2; ++t)
                 if (cnt[t] > 0) drain_wait(&bar.m_full[t], (cnt[t] - 1) & 1, p.timeout_ns);
         }
+    } else if (Cfg::kSplit && (warp == 9 || warp == 11)) {
+        // ------------------------------------------------ MMA issuers, one per query tile
+        // With P in its own columns S_t^{j+1} can be computed as soon as the
+        // softmax warps have read S_t^j, while they still work on it. Warp 9
+        // issues every MMA of query tile 0, warp 11 those of tile 1, so one
+        // issuer's barrier waits overlap the other's MMAs. Each issuer walks every
+        // K/V ring slot (waiting for it to fill) and releases it once, used or not;
+        // the slot's empty barrier expects both.
+        const int t = warp == 9 ? 0 : 1;
+        const uint32_t tS = tmem + t * BN, tO = tmem + 256 + t * D, tP = tmem + 384 + t * 64;
+        uint32_t it = 0, n_units = 0, n_s = 0, n_p = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++n_units) {
+            const Unit w = decode_unit(p, u);
+            const int nkv = w.nkv[t];
+            ok = mbar_wait_warp(&bar.q_full, n_units & 1, wc);
+            if (!ok) break;
+            tc_fence_after();
+            if (nkv == 0) {  // this tile lies beyond N: release Q at once
+                if (elect_one()) mbar_arrive(&bar.q_empty);
+                __syncwarp();
+            }
+            for (int j = 0; j <= w.nkv_max && ok; ++j) {
+                const uint32_t itK = it;  // ring slot of K_j; V_j follows it
+                const uint32_t sK = itK % Cfg::kStages, sV_prev = (itK + Cfg::kStages - 1) % Cfg::kStages;
+                if (j < w.nkv_max) {
+                    ok = mbar_wait_warp(&bar.kv_full[sK], (itK / Cfg::kStages) & 1, wc);
+                    if (!ok) break;
+                    if (j < nkv) {
+                        // S_t^j = Q_t K_j^T, once the softmax warps have read S_t^{j-1}
+                        if (n_s > 0) {
+                            ok = mbar_wait_warp(&bar.s_free[t], (n_s - 1) & 1, wc);
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+                        const uint32_t qt = sQ + t * Cfg::kTileBytes, kt = sKV + sK * Cfg::kTileBytes;
+                        if (elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_ss(tS, kmajor_desc(qt, kk), kmajor_desc(kt, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+                            mma_commit(&bar.s_full[t]);
+                            if (j == nkv - 1) mma_commit(&bar.q_empty);  // last read of Q_t
+                        }
+                        __syncwarp();
+                        ++n_s;
+                    }
+                    if (elect_one()) mma_commit(&bar.kv_empty[sK]);
+                    __syncwarp();
+                }
+                if (j > 0) {  // V_{j-1} lives in the slot before K_j
+                    ok = mbar_wait_warp(&bar.kv_full[sV_prev], ((itK - 1) / Cfg::kStages) & 1, wc);
+                    if (!ok) break;
+                    if (j <= nkv) {
+                        // O_t += P_t^{j-1} V_{j-1}, once the softmax warps have stored P_t^{j-1}
+                        ok = mbar_wait_warp(&bar.p_full[t], n_p & 1, wc);
+                        if (!ok) break;
+                        ++n_p;
+                        tc_fence_after();
+                        const uint32_t vt = sKV + sV_prev * Cfg::kTileBytes;
+                        if (elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < BN / 16; ++kk)
+                                mma_ts(tO, tP + kk * 8, vmajor_desc(vt, kk), Cfg::kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
+                            mma_commit(&bar.pv_done[t]);
+                        }
+                        __syncwarp();
+                    }
+                    if (elect_one()) mma_commit(&bar.kv_empty[sV_prev]);
+                    __syncwarp();
+                }
+                if (j < w.nkv_max) it += 2;
+            }
+        }
+        // every MMA this warp issued completes before TMEM is released
+        if (elect_one()) {
+            mma_commit(&bar.drain[t]);
+            drain_wait(&bar.drain[t], 0, p.timeout_ns);
+        }
+        __syncwarp();
     } else if (warp == 9) {
         // ------------------------------------------------ MMA issuer
         // The whole warp walks the schedule and waits; one elected lane (the same
@@ -351,8 +445,8 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
         }
         // every MMA this warp issued completes before TMEM is released
         if (elect_one()) {
-            mma_commit(&bar.drain);
-            drain_wait(&bar.drain, 0, p.timeout_ns);
+            mma_commit(&bar.drain[0]);
+            drain_wait(&bar.drain[0], 0, p.timeout_ns);
         }
         __syncwarp();
       }
@@ -364,8 +458,9 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + t * BN;
         const uint32_t tO = tmem + lane_off + 256 + t * D;
+        const uint32_t tP = Cfg::kSplit ? tmem + lane_off + 384 + t * 64 : tS;
         const uint8_t* mtile = smem + Cfg::kMaskOff + t * Cfg::kMaskBytes;
-        uint32_t scnt = 0, mcnt = 0, ocnt = 0;
+        uint32_t scnt = 0, mcnt = 0, ocnt = 0, pvcnt = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
             const Unit w = decode_unit(p, u);
@@ -385,6 +480,10 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                 tmem_ld32_at<64>(tS + 64, su);
                 tmem_ld32_at<96>(tS + 96, su);
                 tmem_wait_ld();
+                if (Cfg::kSplit) {  // S_t is in registers: the next S_t may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(&bar.s_free[t]);
+                }
                 const bool diag = p.causal && (j == nkv - 1);
                 const bool tail = (j + 1) * BN > p.N;
                 float cc = p.c;
@@ -426,22 +525,28 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                         if (col >= lim) su[col] = __float_as_uint(-INFINITY);
                     cc = 1.f;
                 }
-                // tile max (in the log2 domain after multiplying by cc): 3-input max, two chains
-                float mxa = fmax3(__uint_as_float(su[0]), __uint_as_float(su[1]), __uint_as_float(su[2]));
-                float mxb = fmax3(__uint_as_float(su[3]), __uint_as_float(su[4]), __uint_as_float(su[5]));
+                // tile max (in the log2 domain after multiplying by cc): 3-input max, eight
+                // independent chains of 16 columns each
+                float mx[8];
 #pragma unroll
-                for (int col = 6; col < BN - 2; col += 4) {
-                    mxa = fmax3(mxa, __uint_as_float(su[col]), __uint_as_float(su[col + 1]));
-                    mxb = fmax3(mxb, __uint_as_float(su[col + 2]), __uint_as_float(su[col + 3]));
+                for (int c = 0; c < 8; ++c) {
+                    float m = fmaxf(__uint_as_float(su[16 * c]), __uint_as_float(su[16 * c + 1]));
+#pragma unroll
+                    for (int e = 2; e < 16; e += 2)
+                        m = fmax3(m, __uint_as_float(su[16 * c + e]), __uint_as_float(su[16 * c + e + 1]));
+                    mx[c] = m;
                 }
-                mxa = fmax3(mxa, __uint_as_float(su[BN - 2]), __uint_as_float(su[BN - 1]));
-                const float m_tile = fmaxf(mxa, mxb) * cc;
+                const float m_tile =
+                    fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], mx[4]), fmax3(mx[5], mx[6], mx[7])) * cc;
                 float m_new = m_ref;
                 if (m_tile > m_ref + kRescaleThreshold) m_new = m_tile;
                 const bool moved = m_new != m_ref;
                 const float alpha = moved ? ex2(m_ref - m_new) : 1.f;  // 0 when m_ref = -inf
-                if (j > 0 && __any_sync(0xffffffffu, moved && m_ref != -INFINITY)) {
-                    // O_t *= alpha (the PV of tile j-1 has completed: it precedes S_t^j)
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, moved && m_ref != -INFINITY);
+                // O_t *= alpha. The PV of key tile j-1 must be complete: here it precedes S_t^j
+                // in the MMA stream (the s_full commit covers it); with P in its own columns
+                // it is the pv_done commit, taken after the exponentials below.
+                auto rescale_o = [&]() {
 #pragma unroll
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t ov[32];
@@ -449,34 +554,61 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
-                            const float2 r = fmul2(make_float2(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])),
-                                                   make_float2(alpha, alpha));
-                            ov[i] = __float_as_uint(r.x);
-                            ov[i + 1] = __float_as_uint(r.y);
+                            const float2 r2 = fmul2(make_float2(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])),
+                                                    make_float2(alpha, alpha));
+                            ov[i] = __float_as_uint(r2.x);
+                            ov[i + 1] = __float_as_uint(r2.y);
                         }
                         tmem_st32(tO + c0, ov);
                     }
-                }
+                };
+                if (!Cfg::kSplit && rescale) rescale_o();
                 m_ref = m_new;
                 const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 // p = 2^(s * cc - m): one packed FMA per pair, two exp2, one packed add, one convert
                 const float2 cc2 = make_float2(cc, cc), nm2 = make_float2(neg_m, neg_m);
                 float2 suma = make_float2(0.f, 0.f), sumb = make_float2(0.f, 0.f);
+                if (Cfg::kSplit) {
+                    // P packed into su[0..63] (pair i lands in su[i], already consumed)
 #pragma unroll
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 x = ffma2(
-                            make_float2(__uint_as_float(su[c0 + 2 * i]), __uint_as_float(su[c0 + 2 * i + 1])), cc2, nm2);
+                    for (int i = 0; i < BN / 2; ++i) {
+                        const float2 x = ffma2(make_float2(__uint_as_float(su[2 * i]), __uint_as_float(su[2 * i + 1])),
+                                               cc2, nm2);
                         const float2 pp = make_float2(ex2(x.x), ex2(x.y));
                         if (i & 1)
                             sumb = fadd2(sumb, pp);
                         else
                             suma = fadd2(suma, pp);
-                        pk[i] = pack_bf16(pp.x, pp.y);
+                        su[i] = pack_bf16(pp.x, pp.y);
                     }
-                    tmem_st16(tS + c0 / 2, pk);
+                    if (j > 0) {  // PV of key tile j-1 has finished reading P_t and writing O_t
+                        ok = mbar_wait(&bar.pv_done[t], pvcnt & 1, wc);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        ++pvcnt;
+                        tc_fence_after();
+                        if (rescale) rescale_o();
+                    }
+                    tmem_st32_at<0>(tP + 0, su);
+                    tmem_st32_at<32>(tP + 32, su);
+                } else {
+#pragma unroll
+                    for (int c0 = 0; c0 < BN; c0 += 32) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 x = ffma2(
+                                make_float2(__uint_as_float(su[c0 + 2 * i]), __uint_as_float(su[c0 + 2 * i + 1])), cc2,
+                                nm2);
+                            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                            if (i & 1)
+                                sumb = fadd2(sumb, pp);
+                            else
+                                suma = fadd2(suma, pp);
+                            pk[i] = pack_bf16(pp.x, pp.y);
+                        }
+                        tmem_st16(tS + c0 / 2, pk);
+                    }
                 }
                 l = l * alpha + ((suma.x + suma.y) + (sumb.x + sumb.y));
                 tmem_wait_st();
@@ -485,10 +617,17 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
             }
             if (!ok) break;
             // epilogue: O = O / l (0 for fully masked rows), LSE in natural log
-            ok = mbar_wait(&bar.o_full[t], ocnt & 1, wc);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ++ocnt;
+            if (Cfg::kSplit) {
+                ok = mbar_wait(&bar.pv_done[t], pvcnt & 1, wc);  // the unit's last PV
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++pvcnt;
+            } else {
+                ok = mbar_wait(&bar.o_full[t], ocnt & 1, wc);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++ocnt;
+            }
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16* orow = p.o + w.b * p.o_sb + w.h * p.o_sh + (long long)row * p.o_sn;
@@ -511,7 +650,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bar.o_empty[t]);
+            if (!Cfg::kSplit) mbar_arrive(&bar.o_empty[t]);
             if (row < p.N)
                 p.lse[((long long)w.b * p.H + w.h) * p.N + row] =
                     l > 0.f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
