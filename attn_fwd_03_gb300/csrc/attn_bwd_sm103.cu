@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(384, 1)
 //   [256,320) dV   [320,384) dK   [384,448) dQ (query rows = lanes)
 //
 // Warps (16): 0-7 P^T / dS^T (two warpgroups, 32 queries of each half each),
-// 8 TMA producer, 9 MMA issuer, 10-11 idle, 12-15 dQ drain. The drain has its
+// 8 TMA producer, 9 and 10 MMA issuers, 11 idle, 12-15 dQ drain. The drain has its
 // own warpgroup so the P^T / dS^T warps move on to the next half at once.
 // ============================================================================
 template <bool MASK>
@@ -455,8 +455,10 @@ struct __align__(8) Bwd64Barriers {
     uint64_t kv_full;
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full[2], ds_ready[2];  // per TMEM buffer
-    uint64_t dq_full, dq_empty, kv_done, drain;
+    uint64_t dq_full, dq_empty, kv_done, drain[2];
     uint64_t dq_staged, dq_free;      // dQ staging in shared memory filled / free again
+    uint64_t buf_free[2];             // dV / dK of the half in a TMEM buffer done reading it
+    uint64_t dq_done[2];              // dQ of the tile in a dS buffer done reading it
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -503,7 +505,11 @@ __global__ void __launch_bounds__(512, 1)
         mbar_init(&bar.dq_full, 1);
         mbar_init(&bar.dq_empty, 128);
         mbar_init(&bar.kv_done, 1);
-        mbar_init(&bar.drain, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.drain[i], 1);
+            mbar_init(&bar.buf_free[i], 1);
+            mbar_init(&bar.dq_done[i], 1);
+        }
         mbar_init(&bar.dq_staged, 128);
         mbar_init(&bar.dq_free, 1);
         fence_mbar_init();
@@ -560,83 +566,96 @@ __global__ void __launch_bounds__(512, 1)
                 drain_wait(&bar.st_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
             drain_wait(&bar.kv_full, 0, p.timeout_ns);
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------ MMA issuer
-        // Converged warp; one elected lane (always the same one) issues MMAs and commits.
+    } else if (warp == 9 || warp == 10) {
+        // ------------------------------------------------ MMA issuers
+        // A tcgen05.mma issue returns only once the tensor core has taken it in,
+        // so an issuer that waits on a barrier leaves the tensor core idle. Two
+        // converged issuer warps, each with one elected lane (always the same
+        // one) issuing its MMAs and commits, keep one issuing while the other
+        // waits: warp 9 the scores S^T, dP^T of every half, warp 10 the
+        // gradients dV, dK of every half and dQ of every tile. Their MMAs do not
+        // run in a common order, so the scores of half u+2 wait until the
+        // gradients of half u have read the TMEM buffer (buf_free), and the
+        // P^T / dS^T warps wait until dQ of tile i has read the dS buffer before
+        // they fill it for tile i+2 (dq_done).
         bool ok = mbar_wait_warp(&bar.kv_full, 0, wc);
         tc_fence_after();
-        // S^T and dP^T of half u into buffer u & 1 (its previous contents were read by
-        // the dV / dK MMAs of half u-2, issued earlier)
-        auto issue_scores = [&](int u) {
-            const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
-            if (hf == 0) {
-                ok = mbar_wait_warp(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
-                if (!ok) return;
-                tc_fence_after();
-            }
-            const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
-            const uint32_t sdO = sQ + Cfg::kTileBytes;
-            if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128 * hf, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128 * hf + 64, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
-                           kk > 0 ? 1u : 0u);
-                mma_commit(&bar.s_full[hf]);
-            }
-            __syncwarp();
-        };
-        // dV, dK of half v, then dQ when v closes a tile (which also releases its stage)
-        auto issue_grads = [&](int v) {
-            const int itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
-            ok = mbar_wait_warp(&bar.ds_ready[hv], (v >> 1) & 1, wc);
-            if (!ok) return;
-            tc_fence_after();
-            const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
-            const uint32_t sdO = sQ + Cfg::kTileBytes;
-            if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tmem + 256, tmem + 128 * hv + half_packed_col(kk), mnmajor_desc(sdO, kk), Cfg::kIdescKV,
-                           (v > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tmem + 320, tmem + 128 * hv + 64 + half_packed_col(kk), mnmajor_desc(sQ, kk),
-                           Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
-            }
-            __syncwarp();
-            if (hv == 1) {
-                if (itv > 0) {  // the previous tile's dQ has been read out of TMEM
-                    ok = mbar_wait_warp(&bar.dq_empty, (itv - 1) & 1, wc);
-                    if (!ok) return;
-                    tc_fence_after();
+        if (warp == 9) {
+            for (int u = 0; u < n_half && ok; ++u) {
+                // S^T and dP^T of half u into buffer u & 1
+                const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
+                if (hf == 0) {
+                    ok = mbar_wait_warp(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+                    if (!ok) break;
                 }
-                const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (itv & 1) * Cfg::kDSBytes);
+                if (u >= 2) {  // dV / dK of half u-2 have read the buffer
+                    ok = mbar_wait_warp(&bar.buf_free[hf], ((u - 2) >> 1) & 1, wc);
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
+                const uint32_t sdO = sQ + Cfg::kTileBytes;
                 if (elect_one()) {
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + 128 * hf, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS,
                                kk > 0 ? 1u : 0u);
-                    mma_commit(&bar.dq_full);
-                    mma_commit(&bar.st_empty[sv]);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + 128 * hf + 64, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
+                               kk > 0 ? 1u : 0u);
+                    mma_commit(&bar.s_full[hf]);
                 }
                 __syncwarp();
             }
-        };
-        for (int u = 0; u <= n_half && ok; ++u) {
-            // With a single stage the next tile's operands can only arrive after the
-            // previous tile released the stage, so its gradient MMAs go first.
-            const bool grads_first = Cfg::kStages == 1 && (u & 1) == 0;
-            if (grads_first && u > 0) issue_grads(u - 1);
-            if (ok && u < n_half) issue_scores(u);
-            if (ok && !grads_first && u > 0) issue_grads(u - 1);
+        } else {
+            for (int v = 0; v < n_half && ok; ++v) {
+                // dV += P^T dO and dK += dS^T Q of half v
+                const int itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
+                ok = mbar_wait_warp(&bar.ds_ready[hv], (v >> 1) & 1, wc);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
+                const uint32_t sdO = sQ + Cfg::kTileBytes;
+                if (elect_one()) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(tmem + 256, tmem + 128 * hv + half_packed_col(kk), mnmajor_desc(sdO, kk),
+                               Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ts(tmem + 320, tmem + 128 * hv + 64 + half_packed_col(kk), mnmajor_desc(sQ, kk),
+                               Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bar.buf_free[hv]);
+                    // the tile's last reads of Q and dO (its scores completed before ds_ready)
+                    if (hv == 1) mma_commit(&bar.st_empty[sv]);
+                }
+                __syncwarp();
+                if (hv == 1) {
+                    // dQ = dS K of the tile, once the drain has read the previous one out of TMEM
+                    if (itv > 0) {
+                        ok = mbar_wait_warp(&bar.dq_empty, (itv - 1) & 1, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (itv & 1) * Cfg::kDSBytes);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
+                                   kk > 0 ? 1u : 0u);
+                        mma_commit(&bar.dq_full);
+                        mma_commit(&bar.dq_done[itv & 1]);
+                    }
+                    __syncwarp();
+                }
+            }
+            if (elect_one() && ok) mma_commit(&bar.kv_done);
+            __syncwarp();
         }
         if (elect_one()) {
-            if (ok) mma_commit(&bar.kv_done);
-            mma_commit(&bar.drain);
-            drain_wait(&bar.drain, 0, p.timeout_ns);
+            mma_commit(&bar.drain[warp - 9]);
+            drain_wait(&bar.drain[warp - 9], 0, p.timeout_ns);
         }
         __syncwarp();
     } else if (warp < 8) {
@@ -692,6 +711,11 @@ __global__ void __launch_bounds__(512, 1)
             // packed pairs go into the first 16 of the 32 columns this thread just read
             tmem_st16(tRow + 128 * hf + 32 * g, pk);
             tmem_st16(tRow + 128 * hf + 64 + 32 * g, dk);
+            if (hf == 0 && it >= 2) {  // dQ of tile it-2 has finished reading this dS buffer
+                ok = mbar_wait(&bar.dq_done[it & 1], ((it - 2) >> 1) & 1, wc);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
             // dS row kr, queries ql0 .. ql0+31 of tile buffer (it & 1): box hf, chunks 4g .. 4g+3
             uint8_t* box = smem + Cfg::kDSOff + (it & 1) * Cfg::kDSBytes + hf * (128 * 128) + kr * 128;
 #pragma unroll
