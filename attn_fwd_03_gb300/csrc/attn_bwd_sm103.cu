@@ -685,8 +685,34 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t sv[32], pv[32];
             tmem_ld32(tRow + 128 * hf + 32 * g, sv);
             tmem_ld32(tRow + 128 * hf + 64 + 32 * g, pv);
+            // before the first half of tile it >= 2 writes the dS buffer, dQ of tile it-2 must
+            // have read it: test now, wait (if still needed) just before the writes
+            const bool need_dq_done = hf == 0 && it >= 2;
+            bool dq_done_seen = !need_dq_done || mbar_test(&bar.dq_done[it & 1], ((it - 2) >> 1) & 1);
             tmem_wait_ld();
             uint32_t pk[16], dk[16];
+            if (!MASK && !diag && key_ok) {
+                // interior tile: no masking
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 nl = *reinterpret_cast<const float4*>(nlv + i);
+                    const float4 nd = *reinterpret_cast<const float4*>(ndv + i);
+                    const float2 x0 =
+                        ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, make_float2(nl.x, nl.y));
+                    const float2 x1 = ffma2(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), c2,
+                                            make_float2(nl.z, nl.w));
+                    const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+                    const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+                    const float2 d0 = fmul2(
+                        p0, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), make_float2(nd.x, nd.y)));
+                    const float2 d1 = fmul2(p1, fadd2(make_float2(__uint_as_float(pv[i + 2]), __uint_as_float(pv[i + 3])),
+                                                      make_float2(nd.z, nd.w)));
+                    pk[i / 2] = pack_bf16(p0.x, p0.y);
+                    pk[i / 2 + 1] = pack_bf16(p1.x, p1.y);
+                    dk[i / 2] = pack_bf16(d0.x, d0.y);
+                    dk[i / 2 + 1] = pack_bf16(d1.x, d1.y);
+                }
+            } else {
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
                 const int q = ql0 + i;
@@ -708,10 +734,11 @@ __global__ void __launch_bounds__(512, 1)
                 pk[i / 2] = pack_bf16(pr.x, pr.y);
                 dk[i / 2] = pack_bf16(ds.x, ds.y);
             }
+            }
             // packed pairs go into the first 16 of the 32 columns this thread just read
             tmem_st16(tRow + 128 * hf + 32 * g, pk);
             tmem_st16(tRow + 128 * hf + 64 + 32 * g, dk);
-            if (hf == 0 && it >= 2) {  // dQ of tile it-2 has finished reading this dS buffer
+            if (!__all_sync(0xffffffffu, dq_done_seen)) {
                 ok = mbar_wait(&bar.dq_done[it & 1], ((it - 2) >> 1) & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
