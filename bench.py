@@ -344,8 +344,9 @@ def run_ours(args, w, rank, world, local_rank):
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     roof = dict(kernels[dom])
     roof.pop("ms")
-    roof.update({"kernel": dom, "traffic": None, "peak_source": peak_src,
-                 "note": "achieved = algorithmic FLOPs per launch / CUDA-event launch duration"})
+    roof.update({"kernel": dom, "traffic": captured_traffic(dom, w.name), "peak_source": peak_src,
+                 "note": "achieved = algorithmic FLOPs per launch / CUDA-event launch duration; traffic = "
+                         "DRAM bytes per launch from an ncu capture of the same kernel source (null if stale)"})
 
     # ---- end to end through the public API with pinned host buffers
     in_names = ("q", "k", "v", "do") if w.backward else ("q", "k", "v")
@@ -419,6 +420,30 @@ def run_ours(args, w, rank, world, local_rank):
                                 "sample": f"{heads} whole head(s) of the workload, fp64 forward+backward, "
                                           f"{el:.1f} s"}
     print(json.dumps(line), flush=True)
+
+
+def captured_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from profiles/dram_traffic.json,
+    or None when there is no capture or the kernel's sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in doc.get("entries", []):
+        if e.get("kernel") != kernel or e.get("workload") != workload:
+            continue
+        for rel, digest in e.get("sources", {}).items():
+            try:
+                with open(os.path.join(ROOT, rel), "rb") as f:
+                    if hashlib.sha256(f.read()).hexdigest() != digest:
+                        return None
+            except OSError:
+                return None
+        return int(e["dram_bytes_read"]) + int(e["dram_bytes_write"])
+    return None
 
 
 def main():
