@@ -414,17 +414,19 @@ __global__ void __launch_bounds__(384, 1)
 //
 // At d = 64 tensor memory has room to overlap the phases the d = 128 kernel
 // runs one after another. Each 128-query tile is processed as two halves of
-// 64 queries; the scores of a half go into one of two TMEM buffers, so while
-// the warpgroups turn half u into P^T / dS^T, the tensor core already runs
-// S^T / dP^T of half u+1 and dV / dK of half u-1. dQ of a whole tile has its
-// own TMEM columns and the dS tile two shared-memory buffers, so the dQ drain
-// is off the critical path too.
+// 64 queries. The tensor core computes the scores S^T, dP^T of half u+2 while
+// the warpgroups turn half u+1 into P^T / dS^T and while it runs dV / dK of
+// half u. dQ of a whole tile has its own TMEM columns and the dS tile two
+// shared-memory buffers, so the dQ drain is off the critical path too.
 //
-// Tensor memory (512 columns):
-//   [128h, 128h+64)       S^T of the half in buffer h (fp32, 64 queries);
-//                         P^T bf16 pairs of warpgroup g's 32 queries at 128h + 32g
-//   [128h+64, 128h+128)   dP^T; dS^T pairs at 128h + 64 + 32g
+// Tensor memory (512 columns, lane = key row), in 64-column slots:
+//   S slots   [0,64) [64,128) [128,192)  S^T of half u in slot u % 3 (fp32, 64 queries);
+//             the warpgroups overwrite it with P^T and dS^T bf16 pairs (warpgroup g:
+//             P^T at 32g + [0,16), dS^T at 32g + [16,32)), which dV / dK read
+//   dP slots  [192,256) [448,512)         dP^T of half u in slot u % 2, free once loaded
 //   [256,320) dV   [320,384) dK   [384,448) dQ (query rows = lanes)
+// A half holds its dP slot only until the warpgroups have loaded it and its S
+// slot until dV / dK have read P^T and dS^T, so three halves are in flight.
 //
 // Warps (16): 0-7 P^T / dS^T (two warpgroups, 32 queries of each half each),
 // 8 TMA producer, 9 and 10 MMA issuers, 11 idle, 12-15 dQ drain. The drain has its
@@ -454,17 +456,22 @@ struct Bwd64Cfg {
 struct __align__(8) Bwd64Barriers {
     uint64_t kv_full;
     uint64_t st_full[2], st_empty[2];
-    uint64_t s_full[2], ds_ready[2];  // per TMEM buffer
+    uint64_t s_full[3], ds_ready[3];  // per S slot
+    uint64_t dp_loaded[2];            // per dP slot: the warpgroups have loaded dP^T
     uint64_t dq_full, dq_empty, kv_done, drain[2];
     uint64_t dq_staged, dq_free;      // dQ staging in shared memory filled / free again
-    uint64_t buf_free[2];             // dV / dK of the half in a TMEM buffer done reading it
+    uint64_t buf_free[3];             // per S slot: dV / dK of its half done reading it
     uint64_t dq_done[2];              // dQ of the tile in a dS buffer done reading it
     uint32_t tmem_base;
     int abort_flag;
 };
 
-// TMEM column, within a buffer, of the bf16 pairs for MMA k-step kk (16 queries) of a half.
+// TMEM column, within an S slot, of the P^T bf16 pairs for MMA k-step kk (16 queries) of a
+// half; dS^T pairs are 16 columns further.
 __host__ __device__ constexpr int half_packed_col(int kk) { return 32 * (kk >> 1) + 8 * (kk & 1); }
+__host__ __device__ constexpr uint32_t s_slot_col(int u) { return 64u * (uint32_t)(u % 3); }
+__host__ __device__ constexpr uint32_t dp_slot_col(int u) { return (u & 1) ? 448u : 192u; }
+static_assert(sizeof(Bwd64Barriers) <= 256, "barrier block");
 
 template <bool MASK>
 __global__ void __launch_bounds__(512, 1)
@@ -499,15 +506,18 @@ __global__ void __launch_bounds__(512, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.st_full[i], 1);
             mbar_init(&bar.st_empty[i], 1);
+            mbar_init(&bar.dp_loaded[i], 256);
+        }
+        for (int i = 0; i < 3; ++i) {
             mbar_init(&bar.s_full[i], 1);
             mbar_init(&bar.ds_ready[i], 256);
+            mbar_init(&bar.buf_free[i], 1);
         }
         mbar_init(&bar.dq_full, 1);
         mbar_init(&bar.dq_empty, 128);
         mbar_init(&bar.kv_done, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.drain[i], 1);
-            mbar_init(&bar.buf_free[i], 1);
             mbar_init(&bar.dq_done[i], 1);
         }
         mbar_init(&bar.dq_staged, 128);
@@ -575,21 +585,26 @@ __global__ void __launch_bounds__(512, 1)
         // waits: warp 9 the scores S^T, dP^T of every half, warp 10 the
         // gradients dV, dK of every half and dQ of every tile. Their MMAs do not
         // run in a common order, so the scores of half u+2 wait until the
-        // gradients of half u have read the TMEM buffer (buf_free), and the
+        // gradients of half u-3 have read its S slot (buf_free) and the warpgroups
+        // have loaded dP^T of half u-2 from its dP slot (dp_loaded), and the
         // P^T / dS^T warps wait until dQ of tile i has read the dS buffer before
         // they fill it for tile i+2 (dq_done).
         bool ok = mbar_wait_warp(&bar.kv_full, 0, wc);
         tc_fence_after();
         if (warp == 9) {
             for (int u = 0; u < n_half && ok; ++u) {
-                // S^T and dP^T of half u into buffer u & 1
+                // S^T of half u into S slot u % 3, dP^T into dP slot u % 2
                 const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
                 if (hf == 0) {
                     ok = mbar_wait_warp(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
                     if (!ok) break;
                 }
-                if (u >= 2) {  // dV / dK of half u-2 have read the buffer
-                    ok = mbar_wait_warp(&bar.buf_free[hf], ((u - 2) >> 1) & 1, wc);
+                if (u >= 3) {  // dV / dK of half u-3 have read the S slot
+                    ok = mbar_wait_warp(&bar.buf_free[u % 3], ((u - 3) / 3) & 1, wc);
+                    if (!ok) break;
+                }
+                if (u >= 2) {  // dP^T of half u-2 has been loaded out of the dP slot
+                    ok = mbar_wait_warp(&bar.dp_loaded[u & 1], ((u - 2) >> 1) & 1, wc);
                     if (!ok) break;
                 }
                 tc_fence_after();
@@ -598,13 +613,13 @@ __global__ void __launch_bounds__(512, 1)
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + 128 * hf, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS,
+                        mma_ss(tmem + s_slot_col(u), kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS,
                                kk > 0 ? 1u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + 128 * hf + 64, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
+                        mma_ss(tmem + dp_slot_col(u), kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
                                kk > 0 ? 1u : 0u);
-                    mma_commit(&bar.s_full[hf]);
+                    mma_commit(&bar.s_full[u % 3]);
                 }
                 __syncwarp();
             }
@@ -612,7 +627,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int v = 0; v < n_half && ok; ++v) {
                 // dV += P^T dO and dK += dS^T Q of half v
                 const int itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
-                ok = mbar_wait_warp(&bar.ds_ready[hv], (v >> 1) & 1, wc);
+                ok = mbar_wait_warp(&bar.ds_ready[v % 3], (v / 3) & 1, wc);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
@@ -620,13 +635,13 @@ __global__ void __launch_bounds__(512, 1)
                 if (elect_one()) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + 256, tmem + 128 * hv + half_packed_col(kk), mnmajor_desc(sdO, kk),
+                        mma_ts(tmem + 256, tmem + s_slot_col(v) + half_packed_col(kk), mnmajor_desc(sdO, kk),
                                Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + 320, tmem + 128 * hv + 64 + half_packed_col(kk), mnmajor_desc(sQ, kk),
+                        mma_ts(tmem + 320, tmem + s_slot_col(v) + 16 + half_packed_col(kk), mnmajor_desc(sQ, kk),
                                Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bar.buf_free[hv]);
+                    mma_commit(&bar.buf_free[v % 3]);
                     // the tile's last reads of Q and dO (its scores completed before ds_ready)
                     if (hv == 1) mma_commit(&bar.st_empty[sv]);
                 }
@@ -670,7 +685,7 @@ __global__ void __launch_bounds__(512, 1)
         for (int u = 0; u < n_half && ok; ++u) {
             const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
             const int q0 = (i_begin + it) * BQ;
-            ok = mbar_wait(&bar.s_full[hf], (u >> 1) & 1, wc);
+            ok = mbar_wait(&bar.s_full[u % 3], (u / 3) & 1, wc);
             ok = ok && mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -683,13 +698,16 @@ __global__ void __launch_bounds__(512, 1)
             const bool key_ok = kg < p.N;
             const uint8_t* mt = stage + 2 * Cfg::kTileBytes;
             uint32_t sv[32], pv[32];
-            tmem_ld32(tRow + 128 * hf + 32 * g, sv);
-            tmem_ld32(tRow + 128 * hf + 64 + 32 * g, pv);
+            const uint32_t tS = tRow + s_slot_col(u) + 32 * g;
+            tmem_ld32(tS, sv);
+            tmem_ld32(tRow + dp_slot_col(u) + 32 * g, pv);
             // before the first half of tile it >= 2 writes the dS buffer, dQ of tile it-2 must
             // have read it: test now, wait (if still needed) just before the writes
             const bool need_dq_done = hf == 0 && it >= 2;
             bool dq_done_seen = !need_dq_done || mbar_test(&bar.dq_done[it & 1], ((it - 2) >> 1) & 1);
             tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bar.dp_loaded[u & 1]);  // the dP slot may take the half after next
             uint32_t pk[16], dk[16];
             if (!MASK && !diag && key_ok) {
                 // interior tile: no masking
@@ -735,9 +753,9 @@ __global__ void __launch_bounds__(512, 1)
                 dk[i / 2] = pack_bf16(ds.x, ds.y);
             }
             }
-            // packed pairs go into the first 16 of the 32 columns this thread just read
-            tmem_st16(tRow + 128 * hf + 32 * g, pk);
-            tmem_st16(tRow + 128 * hf + 64 + 32 * g, dk);
+            // P^T and dS^T pairs go into the 32 S^T columns this thread just read
+            tmem_st16(tS, pk);
+            tmem_st16(tS + 16, dk);
             if (!__all_sync(0xffffffffu, dq_done_seen)) {
                 ok = mbar_wait(&bar.dq_done[it & 1], ((it - 2) >> 1) & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
@@ -754,7 +772,7 @@ __global__ void __launch_bounds__(512, 1)
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bar.ds_ready[hf]);
+            mbar_arrive(&bar.ds_ready[u % 3]);
         }
         // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of this key tile
         if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
