@@ -85,6 +85,7 @@ struct BwdParamsDev {
     long long dk_sb, dk_sh, dk_sn, dv_sb, dv_sh, dv_sn;
     int mask_hb, mask_bb;
     int n_ktiles;
+    int num_units;  // persistent d = 64 kernel: key tiles x heads
     int* err;
     unsigned long long timeout_ns;
 };
@@ -428,6 +429,11 @@ __global__ void __launch_bounds__(384, 1)
 // A half holds its dP slot only until the warpgroups have loaded it and its S
 // slot until dV / dK have read P^T and dS^T, so three halves are in flight.
 //
+// Persistent: one CTA per SM walks units (b, h, key tile) in snake order. K
+// and V are double-buffered across units, so the next unit's K/V load and its
+// first scores overlap the previous unit's last gradients, dQ drain and dV/dK
+// stores.
+//
 // Warps (16): 0-7 P^T / dS^T (two warpgroups, 32 queries of each half each),
 // 8 TMA producer, 9 and 10 MMA issuers, 11 idle, 12-15 dQ drain. The drain has its
 // own warpgroup so the P^T / dS^T warps move on to the next half at once.
@@ -441,9 +447,9 @@ struct Bwd64Cfg {
     static constexpr int kVecOffInStage = 2 * kTileBytes + (MASK ? kMaskBytes : 0);
     static constexpr int kStageBytes = kVecOffInStage + 1024;
     static constexpr int kDSBytes = BQ * BK * 2;  // one dS tile (two 64-query boxes)
-    static constexpr int kKOff = 0;
-    static constexpr int kVOff = kTileBytes;
-    static constexpr int kDSOff = 2 * kTileBytes;  // two dS buffers
+    static constexpr int kKOff = 0;             // K, V of unit n in buffer n & 1: K at kKOff + 2 tiles x buffer
+    static constexpr int kVOff = kTileBytes;    // V right after its K
+    static constexpr int kDSOff = 4 * kTileBytes;  // two dS buffers
     static constexpr int kStageOff = kDSOff + 2 * kDSBytes;
     static constexpr int kStgOff = kStageOff + kStages * kStageBytes;  // dQ staging: 2 boxes of 32 fp32 x 128 rows
     static constexpr int kBarOff = kStgOff + BQ * D * 4;
@@ -454,7 +460,9 @@ struct Bwd64Cfg {
 };
 
 struct __align__(8) Bwd64Barriers {
-    uint64_t kv_full;
+    uint64_t kv_full[2];              // per K/V buffer
+    uint64_t kv_free[2];              // per K/V buffer: both issuers done with its unit's K and V
+    uint64_t dkv_empty;               // the warpgroups have read this unit's dV and dK
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full[3], ds_ready[3];  // per S slot
     uint64_t dp_loaded[2];            // per dP slot: the warpgroups have loaded dP^T
@@ -473,6 +481,30 @@ __host__ __device__ constexpr uint32_t s_slot_col(int u) { return 64u * (uint32_
 __host__ __device__ constexpr uint32_t dp_slot_col(int u) { return (u & 1) ? 448u : 192u; }
 static_assert(sizeof(Bwd64Barriers) <= 256, "barrier block");
 
+// A unit of the d = 64 backward: key tile kt of head (b, h) against all its query tiles.
+struct Unit64 {
+    int b, h, k0, i_begin, n_it;
+};
+// Units are numbered key tile major, so the first units (early key tiles) are the heaviest
+// under causal masking.
+__device__ __forceinline__ Unit64 unit64(const BwdParamsDev& p, int u) {
+    const int bh = p.B * p.H;
+    const int kt = u / bh, r = u % bh;
+    Unit64 w;
+    w.b = r / p.H;
+    w.h = r % p.H;
+    w.k0 = kt * BK;
+    w.i_begin = p.causal ? kt : 0;
+    w.n_it = (p.N + BQ - 1) / BQ - w.i_begin;
+    return w;
+}
+// The k-th unit of this CTA: rows of gridDim.x units dealt left to right on even rows and
+// right to left on odd rows, which evens the per-CTA work when units get lighter.
+__device__ __forceinline__ int bwd_unit_at(int k) {
+    const int g = gridDim.x, i = blockIdx.x;
+    return k * g + ((k & 1) ? g - 1 - i : i);
+}
+
 template <bool MASK>
 __global__ void __launch_bounds__(512, 1)
     bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -485,16 +517,7 @@ __global__ void __launch_bounds__(512, 1)
     Bwd64Barriers& bar = *reinterpret_cast<Bwd64Barriers*>(smem + Cfg::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WaitCtl wc{p.err, &bar.abort_flag, p.timeout_ns};
-
-    // work unit: key tile kt of (b, h); early key tiles first (they see the most query tiles)
-    const int bh = p.B * p.H;
-    const int kt = blockIdx.x / bh;
-    const int b = (blockIdx.x % bh) / p.H, h = blockIdx.x % p.H;
-    const int k0 = kt * BK;
     const int nq_all = (p.N + BQ - 1) / BQ;
-    const int i_begin = p.causal ? kt : 0;
-    const int n_it = nq_all - i_begin;
-    const int n_half = 2 * n_it;
 
     if ((smem_u32(smem) & 1023u) != 0) {  // the swizzled tiles need a 1024-byte aligned base
         if (threadIdx.x == 0) atomicExch(p.err, -7);
@@ -502,7 +525,11 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (threadIdx.x == 0) {
         bar.abort_flag = 0;
-        mbar_init(&bar.kv_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar.kv_full[i], 1);
+            mbar_init(&bar.kv_free[i], 2);
+        }
+        mbar_init(&bar.dkv_empty, 256);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.st_full[i], 1);
             mbar_init(&bar.st_empty[i], 1);
@@ -532,7 +559,6 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bar.tmem_base;
-    const uint32_t sK = smem_u32(smem + Cfg::kKOff), sV = smem_u32(smem + Cfg::kVOff);
 
     if (warp == 8) {
         // ------------------------------------------------ producer
@@ -542,39 +568,52 @@ __global__ void __launch_bounds__(512, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            mbar_arrive_expect_tx(&bar.kv_full, 2 * Cfg::kTileBytes);
-            tma_load_4d(smem + Cfg::kKOff, &tm_k, &bar.kv_full, 0, k0, h, b);
-            tma_load_4d(smem + Cfg::kVOff, &tm_v, &bar.kv_full, 0, k0, h, b);
         }
         __syncwarp();
-        const int hm = p.mask_hb ? h : 0, bm = p.mask_bb ? b : 0;
         bool ok = true;
-        int it = 0;
-        for (; it < n_it && ok; ++it) {
-            const int s = it % Cfg::kStages;
-            ok = mbar_wait_warp(&bar.st_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
-            if (!ok) break;
-            const int q0 = (i_begin + it) * BQ;
-            uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+        int n = 0, gt = 0;
+        for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku), ++n) {
+            const Unit64 w = unit64(p, u);
+            const int kb = n & 1;
+            if (n >= 2) {  // every MMA of unit n-2 that reads this K/V buffer has completed
+                ok = mbar_wait_warp(&bar.kv_free[kb], ((n - 2) >> 1) & 1, wc);
+                if (!ok) break;
+            }
             if (elect_one()) {
-                mbar_arrive_expect_tx(&bar.st_full[s], Cfg::kStageBytes);
-                tma_load_4d(st, &tm_q, &bar.st_full[s], 0, q0, h, b);
-                tma_load_4d(st + Cfg::kTileBytes, &tm_do, &bar.st_full[s], 0, q0, h, b);
-                if (MASK)
-                    for (int bx = 0; bx < 2; ++bx)
-                        tma_load_4d(st + 2 * Cfg::kTileBytes + bx * 128 * 128, &tm_mask, &bar.st_full[s],
-                                    k0 + bx * 64, q0, hm, bm);
-                bulk_load(st + Cfg::kVecOffInStage,
-                          p.stats + ((long long)(b * p.H + h) * nq_all + (i_begin + it)) * 256, 1024,
-                          &bar.st_full[s]);
+                uint8_t* kvb = smem + Cfg::kKOff + kb * 2 * Cfg::kTileBytes;
+                mbar_arrive_expect_tx(&bar.kv_full[kb], 2 * Cfg::kTileBytes);
+                tma_load_4d(kvb, &tm_k, &bar.kv_full[kb], 0, w.k0, w.h, w.b);
+                tma_load_4d(kvb + Cfg::kTileBytes, &tm_v, &bar.kv_full[kb], 0, w.k0, w.h, w.b);
             }
             __syncwarp();
+            const int hm = p.mask_hb ? w.h : 0, bm = p.mask_bb ? w.b : 0;
+            for (int it = 0; it < w.n_it && ok; ++it, ++gt) {
+                const int s = gt % Cfg::kStages;
+                ok = mbar_wait_warp(&bar.st_empty[s], ((gt / Cfg::kStages) & 1) ^ 1, wc);
+                if (!ok) break;
+                const int q0 = (w.i_begin + it) * BQ;
+                uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&bar.st_full[s], Cfg::kStageBytes);
+                    tma_load_4d(st, &tm_q, &bar.st_full[s], 0, q0, w.h, w.b);
+                    tma_load_4d(st + Cfg::kTileBytes, &tm_do, &bar.st_full[s], 0, q0, w.h, w.b);
+                    if (MASK)
+                        for (int bx = 0; bx < 2; ++bx)
+                            tma_load_4d(st + 2 * Cfg::kTileBytes + bx * 128 * 128, &tm_mask, &bar.st_full[s],
+                                        w.k0 + bx * 64, q0, hm, bm);
+                    bulk_load(st + Cfg::kVecOffInStage,
+                              p.stats + ((long long)(w.b * p.H + w.h) * nq_all + (w.i_begin + it)) * 256, 1024,
+                              &bar.st_full[s]);
+                }
+                __syncwarp();
+            }
         }
+        // every copy issued lands before the CTA exits
         if (lane == 0) {
-            const int last = it < Cfg::kStages ? it : Cfg::kStages;
-            for (int i = it - last; i < it; ++i)
+            const int last = gt < Cfg::kStages ? gt : Cfg::kStages;
+            for (int i = gt - last; i < gt; ++i)
                 drain_wait(&bar.st_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
-            drain_wait(&bar.kv_full, 0, p.timeout_ns);
+            for (int i = n > 2 ? n - 2 : 0; i < n; ++i) drain_wait(&bar.kv_full[i & 1], (i >> 1) & 1, p.timeout_ns);
         }
     } else if (warp == 9 || warp == 10) {
         // ------------------------------------------------ MMA issuers
@@ -584,89 +623,108 @@ __global__ void __launch_bounds__(512, 1)
         // one) issuing its MMAs and commits, keep one issuing while the other
         // waits: warp 9 the scores S^T, dP^T of every half, warp 10 the
         // gradients dV, dK of every half and dQ of every tile. Their MMAs do not
-        // run in a common order, so the scores of half u+2 wait until the
+        // run in a common order, so the scores of half u wait until the
         // gradients of half u-3 have read its S slot (buf_free) and the warpgroups
         // have loaded dP^T of half u-2 from its dP slot (dp_loaded), and the
         // P^T / dS^T warps wait until dQ of tile i has read the dS buffer before
-        // they fill it for tile i+2 (dq_done).
-        bool ok = mbar_wait_warp(&bar.kv_full, 0, wc);
-        tc_fence_after();
-        if (warp == 9) {
-            for (int u = 0; u < n_half && ok; ++u) {
-                // S^T of half u into S slot u % 3, dP^T into dP slot u % 2
-                const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
-                if (hf == 0) {
-                    ok = mbar_wait_warp(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
-                    if (!ok) break;
-                }
-                if (u >= 3) {  // dV / dK of half u-3 have read the S slot
-                    ok = mbar_wait_warp(&bar.buf_free[u % 3], ((u - 3) / 3) & 1, wc);
-                    if (!ok) break;
-                }
-                if (u >= 2) {  // dP^T of half u-2 has been loaded out of the dP slot
-                    ok = mbar_wait_warp(&bar.dp_loaded[u & 1], ((u - 2) >> 1) & 1, wc);
-                    if (!ok) break;
-                }
-                tc_fence_after();
-                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
-                const uint32_t sdO = sQ + Cfg::kTileBytes;
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + s_slot_col(u), kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS,
-                               kk > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + dp_slot_col(u), kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
-                               kk > 0 ? 1u : 0u);
-                    mma_commit(&bar.s_full[u % 3]);
-                }
-                __syncwarp();
-            }
-        } else {
-            for (int v = 0; v < n_half && ok; ++v) {
-                // dV += P^T dO and dK += dS^T Q of half v
-                const int itv = v >> 1, hv = v & 1, sv = itv % Cfg::kStages;
-                ok = mbar_wait_warp(&bar.ds_ready[v % 3], (v / 3) & 1, wc);
+        // they fill it for tile i+2 (dq_done). Halves and tiles are counted over
+        // all units of the CTA.
+        bool ok = true;
+        int n = 0, gu = 0;
+        for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku), ++n) {
+            const Unit64 w = unit64(p, u);
+            ok = mbar_wait_warp(&bar.kv_full[n & 1], (n >> 1) & 1, wc);
+            if (!ok) break;
+            const uint32_t sK = smem_u32(smem + Cfg::kKOff + (n & 1) * 2 * Cfg::kTileBytes);
+            const uint32_t sV = sK + Cfg::kTileBytes;
+            if (warp == 10 && n > 0) {  // the warpgroups have read dV / dK of the previous unit
+                ok = mbar_wait_warp(&bar.dkv_empty, (n - 1) & 1, wc);
                 if (!ok) break;
-                tc_fence_after();
-                const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
-                const uint32_t sdO = sQ + Cfg::kTileBytes;
-                if (elect_one()) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + 256, tmem + s_slot_col(v) + half_packed_col(kk), mnmajor_desc(sdO, kk),
-                               Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ts(tmem + 320, tmem + s_slot_col(v) + 16 + half_packed_col(kk), mnmajor_desc(sQ, kk),
-                               Cfg::kIdescKV, (v > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bar.buf_free[v % 3]);
-                    // the tile's last reads of Q and dO (its scores completed before ds_ready)
-                    if (hv == 1) mma_commit(&bar.st_empty[sv]);
-                }
-                __syncwarp();
-                if (hv == 1) {
-                    // dQ = dS K of the tile, once the drain has read the previous one out of TMEM
-                    if (itv > 0) {
-                        ok = mbar_wait_warp(&bar.dq_empty, (itv - 1) & 1, wc);
+            }
+            tc_fence_after();
+            const int n_half = 2 * w.n_it;
+            if (warp == 9) {
+                for (int hl = 0; hl < n_half && ok; ++hl, ++gu) {
+                    // S^T of half gu into S slot gu % 3, dP^T into dP slot gu % 2
+                    const int gt = gu >> 1, hf = gu & 1, s = gt % Cfg::kStages;
+                    if (hf == 0) {
+                        ok = mbar_wait_warp(&bar.st_full[s], (gt / Cfg::kStages) & 1, wc);
                         if (!ok) break;
-                        tc_fence_after();
                     }
-                    const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (itv & 1) * Cfg::kDSBytes);
+                    if (gu >= 3) {  // dV / dK of half gu-3 have read the S slot
+                        ok = mbar_wait_warp(&bar.buf_free[gu % 3], ((gu - 3) / 3) & 1, wc);
+                        if (!ok) break;
+                    }
+                    if (gu >= 2) {  // dP^T of half gu-2 has been loaded out of the dP slot
+                        ok = mbar_wait_warp(&bar.dp_loaded[gu & 1], ((gu - 2) >> 1) & 1, wc);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes) + hf * 64 * 128;
+                    const uint32_t sdO = sQ + Cfg::kTileBytes;
                     if (elect_one()) {
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss(tmem + s_slot_col(gu), kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS,
                                    kk > 0 ? 1u : 0u);
-                        mma_commit(&bar.dq_full);
-                        mma_commit(&bar.dq_done[itv & 1]);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss(tmem + dp_slot_col(gu), kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
+                                   kk > 0 ? 1u : 0u);
+                        mma_commit(&bar.s_full[gu % 3]);
                     }
                     __syncwarp();
                 }
+                if (elect_one() && ok) mma_commit(&bar.kv_free[n & 1]);  // this unit's reads of K and V
+                __syncwarp();
+            } else {
+                for (int vl = 0; vl < n_half && ok; ++vl, ++gu) {
+                    // dV += P^T dO and dK += dS^T Q of half gu
+                    const int gt = gu >> 1, hv = gu & 1, sv = gt % Cfg::kStages;
+                    ok = mbar_wait_warp(&bar.ds_ready[gu % 3], (gu / 3) & 1, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + sv * Cfg::kStageBytes) + hv * 64 * 128;
+                    const uint32_t sdO = sQ + Cfg::kTileBytes;
+                    if (elect_one()) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts(tmem + 256, tmem + s_slot_col(gu) + half_packed_col(kk), mnmajor_desc(sdO, kk),
+                                   Cfg::kIdescKV, (vl > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts(tmem + 320, tmem + s_slot_col(gu) + 16 + half_packed_col(kk),
+                                   mnmajor_desc(sQ, kk), Cfg::kIdescKV, (vl > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bar.buf_free[gu % 3]);
+                        // the tile's last reads of Q and dO (its scores completed before ds_ready)
+                        if (hv == 1) mma_commit(&bar.st_empty[sv]);
+                    }
+                    __syncwarp();
+                    if (hv == 1) {
+                        // dQ = dS K of the tile, once the drain has read the previous one out of TMEM
+                        if (gt > 0) {
+                            ok = mbar_wait_warp(&bar.dq_empty, (gt - 1) & 1, wc);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        const uint32_t sDS = smem_u32(smem + Cfg::kDSOff + (gt & 1) * Cfg::kDSBytes);
+                        if (elect_one()) {
+#pragma unroll
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
+                                       kk > 0 ? 1u : 0u);
+                            mma_commit(&bar.dq_full);
+                            mma_commit(&bar.dq_done[gt & 1]);
+                        }
+                        __syncwarp();
+                    }
+                }
+                if (elect_one() && ok) {
+                    mma_commit(&bar.kv_done);  // dV and dK of this unit are complete
+                    mma_commit(&bar.kv_free[n & 1]);  // and its dQ products have read K
+                }
+                __syncwarp();
             }
-            if (elect_one() && ok) mma_commit(&bar.kv_done);
-            __syncwarp();
         }
         if (elect_one()) {
             mma_commit(&bar.drain[warp - 9]);
@@ -674,120 +732,128 @@ __global__ void __launch_bounds__(512, 1)
         }
         __syncwarp();
     } else if (warp < 8) {
-        // ------------------------------------------------ P^T, dS^T (thread = key row), dQ drain
+        // ------------------------------------------------ P^T, dS^T (thread = key row), dV / dK out
         const int g = warp >> 2;  // this warpgroup's 32 queries of each half
         const int kr = (warp & 3) * 32 + lane;
-        const int kg = k0 + kr;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tRow = tmem + lane_off;
         const float2 c2 = make_float2(p.c, p.c);
         bool ok = true;
-        for (int u = 0; u < n_half && ok; ++u) {
-            const int it = u >> 1, hf = u & 1, s = it % Cfg::kStages;
-            const int q0 = (i_begin + it) * BQ;
-            ok = mbar_wait(&bar.s_full[u % 3], (u / 3) & 1, wc);
-            ok = ok && mbar_wait(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
+        int n = 0, gu = 0;
+        for (int ku = 0, uu = bwd_unit_at(0); uu < p.num_units && ok; uu = bwd_unit_at(++ku), ++n) {
+            const Unit64 w = unit64(p, uu);
+            const int kg = w.k0 + kr;
+            const bool key_ok = kg < p.N;
+            const int n_half = 2 * w.n_it;
+            for (int hl = 0; hl < n_half && ok; ++hl, ++gu) {
+                const int gt = gu >> 1, hf = gu & 1, s = gt % Cfg::kStages;
+                const int q0 = (w.i_begin + (hl >> 1)) * BQ;
+                ok = mbar_wait(&bar.s_full[gu % 3], (gu / 3) & 1, wc);
+                ok = ok && mbar_wait(&bar.st_full[s], (gt / Cfg::kStages) & 1, wc);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const uint8_t* stage = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+                const int ql0 = 64 * hf + 32 * g;  // first query (within the tile) of this warpgroup's chunk
+                const float* nlv = reinterpret_cast<const float*>(stage + Cfg::kVecOffInStage) + ql0;  // -LSE*log2e
+                const float* ndv = nlv + 128;                                                            // -D
+                const bool diag = p.causal && (q0 == w.k0);
+                const uint8_t* mt = stage + 2 * Cfg::kTileBytes;
+                uint32_t sv[32], pv[32];
+                const uint32_t tS = tRow + s_slot_col(gu) + 32 * g;
+                tmem_ld32(tS, sv);
+                tmem_ld32(tRow + dp_slot_col(gu) + 32 * g, pv);
+                // before the first half of tile gt >= 2 writes the dS buffer, dQ of tile gt-2 must
+                // have read it: test now, wait (if still needed) just before the writes
+                const bool need_dq_done = hf == 0 && gt >= 2;
+                bool dq_done_seen = !need_dq_done || mbar_test(&bar.dq_done[gt & 1], ((gt - 2) >> 1) & 1);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bar.dp_loaded[gu & 1]);  // the dP slot may take the half after next
+                uint32_t pk[16], dk[16];
+                if (!MASK && !diag && key_ok) {
+                    // interior tile: no masking
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 nl = *reinterpret_cast<const float4*>(nlv + i);
+                        const float4 nd = *reinterpret_cast<const float4*>(ndv + i);
+                        const float2 x0 = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2,
+                                                make_float2(nl.x, nl.y));
+                        const float2 x1 = ffma2(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])),
+                                                c2, make_float2(nl.z, nl.w));
+                        const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+                        const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+                        const float2 d0 = fmul2(p0, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])),
+                                                          make_float2(nd.x, nd.y)));
+                        const float2 d1 = fmul2(
+                            p1, fadd2(make_float2(__uint_as_float(pv[i + 2]), __uint_as_float(pv[i + 3])),
+                                      make_float2(nd.z, nd.w)));
+                        pk[i / 2] = pack_bf16(p0.x, p0.y);
+                        pk[i / 2 + 1] = pack_bf16(p1.x, p1.y);
+                        dk[i / 2] = pack_bf16(d0.x, d0.y);
+                        dk[i / 2 + 1] = pack_bf16(d1.x, d1.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const int q = ql0 + i;
+                        const float2 nl = *reinterpret_cast<const float2*>(nlv + i);
+                        const float2 nd = *reinterpret_cast<const float2*>(ndv + i);
+                        float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl);
+                        if (MASK) {
+                            const int kb = kr >> 6, kc = (kr & 63) >> 3;
+                            const float m0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                mt + kb * 128 * 128 + q * 128 + ((kc ^ (q & 7)) << 4) + (kr & 7) * 2));
+                            const float m1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                mt + kb * 128 * 128 + (q + 1) * 128 + ((kc ^ ((q + 1) & 7)) << 4) + (kr & 7) * 2));
+                            x = ffma2(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
+                        }
+                        if (!key_ok || (diag && q < kr)) x.x = -INFINITY;
+                        if (!key_ok || (diag && q + 1 < kr)) x.y = -INFINITY;
+                        const float2 pr = make_float2(ex2(x.x), ex2(x.y));
+                        const float2 ds =
+                            fmul2(pr, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd));
+                        pk[i / 2] = pack_bf16(pr.x, pr.y);
+                        dk[i / 2] = pack_bf16(ds.x, ds.y);
+                    }
+                }
+                // P^T and dS^T pairs go into the 32 S^T columns this thread just read
+                tmem_st16(tS, pk);
+                tmem_st16(tS + 16, dk);
+                if (!__all_sync(0xffffffffu, dq_done_seen)) {
+                    ok = mbar_wait(&bar.dq_done[gt & 1], ((gt - 2) >> 1) & 1, wc);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
+                // dS row kr, queries ql0 .. ql0+31 of tile buffer (gt & 1): box hf, chunks 4g .. 4g+3
+                uint8_t* box = smem + Cfg::kDSOff + (gt & 1) * Cfg::kDSBytes + hf * (128 * 128) + kr * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int ch = 4 * g + j;
+                    *reinterpret_cast<uint4*>(box + ((ch ^ (kr & 7)) << 4)) =
+                        make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
+                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bar.ds_ready[gu % 3]);
+            }
+            if (!ok) break;
+            // unit epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of
+            // this key tile, then the accumulators are free for the next unit
+            ok = mbar_wait(&bar.kv_done, n & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint8_t* stage = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
-            const int ql0 = 64 * hf + 32 * g;  // first query (within the tile) of this warpgroup's chunk
-            const float* nlv = reinterpret_cast<const float*>(stage + Cfg::kVecOffInStage) + ql0;  // -LSE*log2e
-            const float* ndv = nlv + 128;                                                            // -D
-            const bool diag = p.causal && (q0 == k0);
-            const bool key_ok = kg < p.N;
-            const uint8_t* mt = stage + 2 * Cfg::kTileBytes;
-            uint32_t sv[32], pv[32];
-            const uint32_t tS = tRow + s_slot_col(u) + 32 * g;
-            tmem_ld32(tS, sv);
-            tmem_ld32(tRow + dp_slot_col(u) + 32 * g, pv);
-            // before the first half of tile it >= 2 writes the dS buffer, dQ of tile it-2 must
-            // have read it: test now, wait (if still needed) just before the writes
-            const bool need_dq_done = hf == 0 && it >= 2;
-            bool dq_done_seen = !need_dq_done || mbar_test(&bar.dq_done[it & 1], ((it - 2) >> 1) & 1);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bar.dp_loaded[u & 1]);  // the dP slot may take the half after next
-            uint32_t pk[16], dk[16];
-            if (!MASK && !diag && key_ok) {
-                // interior tile: no masking
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 nl = *reinterpret_cast<const float4*>(nlv + i);
-                    const float4 nd = *reinterpret_cast<const float4*>(ndv + i);
-                    const float2 x0 =
-                        ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, make_float2(nl.x, nl.y));
-                    const float2 x1 = ffma2(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), c2,
-                                            make_float2(nl.z, nl.w));
-                    const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
-                    const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-                    const float2 d0 = fmul2(
-                        p0, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), make_float2(nd.x, nd.y)));
-                    const float2 d1 = fmul2(p1, fadd2(make_float2(__uint_as_float(pv[i + 2]), __uint_as_float(pv[i + 3])),
-                                                      make_float2(nd.z, nd.w)));
-                    pk[i / 2] = pack_bf16(p0.x, p0.y);
-                    pk[i / 2 + 1] = pack_bf16(p1.x, p1.y);
-                    dk[i / 2] = pack_bf16(d0.x, d0.y);
-                    dk[i / 2 + 1] = pack_bf16(d1.x, d1.y);
-                }
-            } else {
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const int q = ql0 + i;
-                const float2 nl = *reinterpret_cast<const float2*>(nlv + i);
-                const float2 nd = *reinterpret_cast<const float2*>(ndv + i);
-                float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl);
-                if (MASK) {
-                    const int kb = kr >> 6, kc = (kr & 63) >> 3;
-                    const float m0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                        mt + kb * 128 * 128 + q * 128 + ((kc ^ (q & 7)) << 4) + (kr & 7) * 2));
-                    const float m1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                        mt + kb * 128 * 128 + (q + 1) * 128 + ((kc ^ ((q + 1) & 7)) << 4) + (kr & 7) * 2));
-                    x = ffma2(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
-                }
-                if (!key_ok || (diag && q < kr)) x.x = -INFINITY;
-                if (!key_ok || (diag && q + 1 < kr)) x.y = -INFINITY;
-                const float2 pr = make_float2(ex2(x.x), ex2(x.y));
-                const float2 ds = fmul2(pr, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd));
-                pk[i / 2] = pack_bf16(pr.x, pr.y);
-                dk[i / 2] = pack_bf16(ds.x, ds.y);
-            }
-            }
-            // P^T and dS^T pairs go into the 32 S^T columns this thread just read
-            tmem_st16(tS, pk);
-            tmem_st16(tS + 16, dk);
-            if (!__all_sync(0xffffffffu, dq_done_seen)) {
-                ok = mbar_wait(&bar.dq_done[it & 1], ((it - 2) >> 1) & 1, wc);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-            }
-            // dS row kr, queries ql0 .. ql0+31 of tile buffer (it & 1): box hf, chunks 4g .. 4g+3
-            uint8_t* box = smem + Cfg::kDSOff + (it & 1) * Cfg::kDSBytes + hf * (128 * 128) + kr * 128;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int ch = 4 * g + j;
-                *reinterpret_cast<uint4*>(box + ((ch ^ (kr & 7)) << 4)) =
-                    make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar.ds_ready[u % 3]);
-        }
-        // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of this key tile
-        if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            tc_fence_after();
-            __nv_bfloat16* dst_row = g == 0 ? p.dv + b * p.dv_sb + h * p.dv_sh + (long long)kg * p.dv_sn
-                                            : p.dk + b * p.dk_sb + h * p.dk_sh + (long long)kg * p.dk_sn;
+            __nv_bfloat16* dst_row = g == 0 ? p.dv + w.b * p.dv_sb + w.h * p.dv_sh + (long long)kg * p.dv_sn
+                                            : p.dk + w.b * p.dk_sb + w.h * p.dk_sh + (long long)kg * p.dk_sn;
             const float mul = g == 0 ? 1.f : p.scale;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tRow + 256 + g * D + c0, v);
                 tmem_wait_ld();
-                if (kg < p.N) {
+                if (key_ok) {
                     uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
@@ -798,6 +864,8 @@ __global__ void __launch_bounds__(512, 1)
                             pack_bf16(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&bar.dkv_empty);
         }
     }
 
@@ -813,46 +881,50 @@ __global__ void __launch_bounds__(512, 1)
         const bool issuer = threadIdx.x == 384;
         if (issuer) prefetch_tmap(&tm_dq);
         bool ok = true;
-        for (int it = 0; it < n_it && ok; ++it) {
-            ok = mbar_wait(&bar.dq_full, it & 1, wc);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t v[64];
-            tmem_ld32_at<0>(tRow + 384, v);
-            tmem_ld32_at<32>(tRow + 416, v);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bar.dq_empty);
-            if (it > 0) {  // the previous tile's reduction has finished reading the staging area
-                ok = mbar_wait(&bar.dq_free, (it - 1) & 1, wc);
+        int gt = 0;
+        for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku)) {
+            const Unit64 w = unit64(p, u);
+            for (int it = 0; it < w.n_it && ok; ++it, ++gt) {
+                ok = mbar_wait(&bar.dq_full, gt & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-            }
-#pragma unroll
-            for (int bx = 0; bx < 2; ++bx) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int col = 32 * bx + 4 * c;
-                    const float2 a0 = fmul2(make_float2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])),
-                                            make_float2(p.scale, p.scale));
-                    const float2 a1 = fmul2(make_float2(__uint_as_float(v[col + 2]), __uint_as_float(v[col + 3])),
-                                            make_float2(p.scale, p.scale));
-                    *reinterpret_cast<float4*>(stg + bx * (BQ * 128) + qr * 128 + ((c ^ (qr & 7)) << 4)) =
-                        make_float4(a0.x, a0.y, a1.x, a1.y);
+                tc_fence_after();
+                uint32_t v[64];
+                tmem_ld32_at<0>(tRow + 384, v);
+                tmem_ld32_at<32>(tRow + 416, v);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&bar.dq_empty);
+                if (gt > 0) {  // the previous tile's reduction has finished reading the staging area
+                    ok = mbar_wait(&bar.dq_free, (gt - 1) & 1, wc);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
                 }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&bar.dq_staged);
-            if (issuer) {
-                ok = mbar_wait(&bar.dq_staged, it & 1, wc);
-                if (ok) {
-                    const int q0 = (i_begin + it) * BQ;
-                    tma_reduce_add_4d(&tm_dq, stg, 0, q0, h, b);
-                    tma_reduce_add_4d(&tm_dq, stg + BQ * 128, 32, q0, h, b);
-                    bulk_commit();
-                    bulk_wait_read0();
-                    mbar_arrive(&bar.dq_free);
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int col = 32 * bx + 4 * c;
+                        const float2 a0 = fmul2(make_float2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])),
+                                                make_float2(p.scale, p.scale));
+                        const float2 a1 = fmul2(make_float2(__uint_as_float(v[col + 2]), __uint_as_float(v[col + 3])),
+                                                make_float2(p.scale, p.scale));
+                        *reinterpret_cast<float4*>(stg + bx * (BQ * 128) + qr * 128 + ((c ^ (qr & 7)) << 4)) =
+                            make_float4(a0.x, a0.y, a1.x, a1.y);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bar.dq_staged);
+                if (issuer) {
+                    ok = mbar_wait(&bar.dq_staged, gt & 1, wc);
+                    if (ok) {
+                        const int q0 = (w.i_begin + it) * BQ;
+                        tma_reduce_add_4d(&tm_dq, stg, 0, q0, w.h, w.b);
+                        tma_reduce_add_4d(&tm_dq, stg + BQ * 128, 32, q0, w.h, w.b);
+                        bulk_commit();
+                        bulk_wait_read0();
+                        mbar_arrive(&bar.dq_free);
+                    }
                 }
             }
         }
@@ -896,7 +968,10 @@ cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, con
     p.n_ktiles = (f.N + BK - 1) / BK;
     p.err = lc.err;
     p.timeout_ns = lc.timeout_ns;
-    const unsigned grid = (unsigned)(p.n_ktiles * f.B * f.H);
+    p.num_units = p.n_ktiles * f.B * f.H;
+    // d = 64: persistent, one CTA per SM walking the units; d = 128: one CTA per unit
+    const unsigned grid = D == 64 ? (unsigned)(p.num_units < lc.num_sms ? p.num_units : lc.num_sms)
+                                  : (unsigned)p.num_units;
     kernel<<<grid, D == 64 ? 512 : 384, kSmem, s>>>(maps.q, maps.k, maps.v, maps.dout, maps.mask, maps.dq_acc, p);
     return cudaGetLastError();
 }
