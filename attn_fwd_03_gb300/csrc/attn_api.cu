@@ -199,6 +199,8 @@ attn_status_t build_bwd_maps(const attn_bwd_params& p, BwdMaps* m) {
     m->v = f.v;
     m->mask = f.mask;
     const uint64_t N = (uint64_t)p.fwd.N, d = (uint64_t)p.fwd.d;
+    if ((st = encode_bf16_map(&m->dk, "dk", p.dk, d, N, p.fwd.H, p.fwd.B, p.dk_stride, 128)) != ATTN_OK) return st;
+    if ((st = encode_bf16_map(&m->dv, "dv", p.dv, d, N, p.fwd.H, p.fwd.B, p.dv_stride, 128)) != ATTN_OK) return st;
     return encode_bf16_map(&m->dout, "dout", p.dout, d, N, p.fwd.H, p.fwd.B, p.do_stride, 128);
 }
 

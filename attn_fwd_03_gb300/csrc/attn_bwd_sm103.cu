@@ -128,7 +128,8 @@ template <int D, bool MASK>
 __global__ void __launch_bounds__(384, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_mask, const __grid_constant__ CUtensorMap tm_dq,
+                  const __grid_constant__ CUtensorMap tm_mask, const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                  const __grid_constant__ CUtensorMap tm_dv,
                   const BwdParamsDev p) {
     using Cfg = BwdCfg<D, MASK>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -463,6 +464,7 @@ struct __align__(8) Bwd64Barriers {
     uint64_t kv_full[2];              // per K/V buffer
     uint64_t kv_free[2];              // per K/V buffer: both issuers done with its unit's K and V
     uint64_t dkv_empty;               // the warpgroups have read this unit's dV and dK
+    uint64_t epi_staged, epi_free;    // dV / dK tile staged in shared memory / TMA store done reading it
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full[3], ds_ready[3];  // per S slot
     uint64_t dp_loaded[2];            // per dP slot: the warpgroups have loaded dP^T
@@ -510,6 +512,7 @@ __global__ void __launch_bounds__(512, 1)
     bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_mask, const __grid_constant__ CUtensorMap tm_dq,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const BwdParamsDev p) {
     using Cfg = Bwd64Cfg<MASK>;
     constexpr int D = 64;
@@ -530,6 +533,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&bar.kv_free[i], 2);
         }
         mbar_init(&bar.dkv_empty, 256);
+        mbar_init(&bar.epi_staged, 256);
+        mbar_init(&bar.epi_free, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.st_full[i], 1);
             mbar_init(&bar.st_empty[i], 1);
@@ -839,34 +844,50 @@ __global__ void __launch_bounds__(512, 1)
                 mbar_arrive(&bar.ds_ready[gu % 3]);
             }
             if (!ok) break;
-            // unit epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of
-            // this key tile, then the accumulators are free for the next unit
+            // unit epilogue: warpgroup 0 stages the dV rows, warpgroup 1 the scale * dK rows of
+            // this key tile in shared memory, and one thread stores both tiles with TMA
+            // (per-thread row stores would write 16 bytes to each of 32 rows per instruction).
+            // The staging area is the dS buffer of the unit's second-to-last tile, whose dQ
+            // product has read it; the next tile to write that buffer is this unit's successor's
+            // first, after the stores have read it (epi_free).
             ok = mbar_wait(&bar.kv_done, n & 1, wc);
+            const int gl = gu / 2 - 1;  // this unit's last tile
+            if (gl >= 1) ok = ok && mbar_wait(&bar.dq_done[(gl - 1) & 1], ((gl - 1) >> 1) & 1, wc);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            __nv_bfloat16* dst_row = g == 0 ? p.dv + w.b * p.dv_sb + w.h * p.dv_sh + (long long)kg * p.dv_sn
-                                            : p.dk + w.b * p.dk_sb + w.h * p.dk_sh + (long long)kg * p.dk_sn;
+            uint32_t v[64];
+            tmem_ld32_at<0>(tRow + 256 + g * D, v);
+            tmem_ld32_at<32>(tRow + 256 + g * D + 32, v);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bar.dkv_empty);  // the accumulators may take the next unit
             const float mul = g == 0 ? 1.f : p.scale;
+            uint8_t* epi = smem + Cfg::kDSOff + ((gl + 1) & 1) * Cfg::kDSBytes + g * (128 * 128) + kr * 128;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tRow + 256 + g * D + c0, v);
-                tmem_wait_ld();
-                if (key_ok) {
-                    uint4* dst = reinterpret_cast<uint4*>(dst_row + c0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(
-                            pack_bf16(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
-                            pack_bf16(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
-                            pack_bf16(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
-                            pack_bf16(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(epi + ((c ^ (kr & 7)) << 4)) = make_uint4(
+                    pack_bf16(__uint_as_float(v[8 * c + 0]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
+                    pack_bf16(__uint_as_float(v[8 * c + 2]) * mul, __uint_as_float(v[8 * c + 3]) * mul),
+                    pack_bf16(__uint_as_float(v[8 * c + 4]) * mul, __uint_as_float(v[8 * c + 5]) * mul),
+                    pack_bf16(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
+            fence_proxy_async_smem();
+            mbar_arrive(&bar.epi_staged);
+            if (threadIdx.x == 0) {  // rows beyond N are clipped by the tensor maps
+                ok = mbar_wait(&bar.epi_staged, n & 1, wc);
+                if (ok) {
+                    const uint8_t* stg0 = smem + Cfg::kDSOff + ((gl + 1) & 1) * Cfg::kDSBytes;
+                    tma_store_4d(&tm_dv, stg0, 0, w.k0, w.h, w.b);
+                    tma_store_4d(&tm_dk, stg0 + 128 * 128, 0, w.k0, w.h, w.b);
+                    bulk_commit();
+                    bulk_wait_read0();
+                    mbar_arrive(&bar.epi_free);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&bar.dkv_empty);
+            ok = mbar_wait(&bar.epi_free, n & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
         }
+        if (threadIdx.x == 0) bulk_wait0();  // the dV / dK stores complete before the CTA exits
     }
 
     else if (warp >= 12) {
@@ -972,7 +993,8 @@ cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, con
     // d = 64: persistent, one CTA per SM walking the units; d = 128: one CTA per unit
     const unsigned grid = D == 64 ? (unsigned)(p.num_units < lc.num_sms ? p.num_units : lc.num_sms)
                                   : (unsigned)p.num_units;
-    kernel<<<grid, D == 64 ? 512 : 384, kSmem, s>>>(maps.q, maps.k, maps.v, maps.dout, maps.mask, maps.dq_acc, p);
+    kernel<<<grid, D == 64 ? 512 : 384, kSmem, s>>>(maps.q, maps.k, maps.v, maps.dout, maps.mask, maps.dq_acc,
+                                                     maps.dk, maps.dv, p);
     return cudaGetLastError();
 }
 

@@ -30,6 +30,7 @@ struct FwdMaps {
 struct BwdMaps {
     CUtensorMap q, k, v, dout, mask;
     CUtensorMap dq_acc;  // fp32 view of the workspace's dQ accumulator (32 x 128 boxes, 128-byte swizzle)
+    CUtensorMap dk, dv;  // outputs (64 x 128 boxes, 128-byte swizzle) for TMA stores of dK / dV tiles
 };
 
 // The two parts of the backward workspace.
