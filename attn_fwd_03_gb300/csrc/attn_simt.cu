@@ -165,79 +165,107 @@ __device__ __forceinline__ bool aligned16(const void* p, int* err) {
     return false;
 }
 
-template <int D>
+// Both kernels below are bound by HBM bandwidth. A thread covers 8 elements of a
+// row (16-byte accesses) for kRowsPerThread rows spaced one grid apart, so each
+// thread keeps several independent loads in flight; row decomposition uses
+// 32-bit arithmetic when the row count allows it (IDX = unsigned), else 64-bit.
+constexpr int kRowsPerThread = 4;
+
+template <int D, typename IDX>
 __global__ void __launch_bounds__(256) bwd_prepass_kernel(SimtArgs a, float* stats, float* dq_acc, int* err) {
-    constexpr int G = D / 8;
-    const int n_pad = (a.N + 127) / 128 * 128;
-    const long long rows = (long long)a.B * a.H * n_pad;
-    const long long prow = (long long)blockIdx.x * (256 / G) + threadIdx.x / G;
+    constexpr int G = D / 8;            // threads per row
+    constexpr int RPB = 256 / G;        // rows per block and step
+    const IDX n_pad = (IDX)((a.N + 127) / 128 * 128);
+    const IDX rows = (IDX)a.B * (IDX)a.H * n_pad;
+    const IDX step = (IDX)gridDim.x * RPB;
     const int part = threadIdx.x % G;
-    const int n = (int)(prow % n_pad);
-    const long long bh = prow / n_pad;
-    float sum = 0.f;
-    bool ok = prow < rows && n < a.N;
-    const __nv_bfloat16 *op = nullptr, *gp = nullptr;
-    float* zp = nullptr;
-    if (ok) {
-        const int h = (int)(bh % a.H);
-        const int b = (int)(bh / a.H);
-        op = row_ptr<__nv_bfloat16>(a.o, b, h, n) + part * 8;
-        gp = row_ptr<__nv_bfloat16>(a.dout, b, h, n) + part * 8;
-        zp = dq_acc + (bh * a.N + n) * D + part * 8;
-        ok = aligned16(op, err) && aligned16(gp, err) && aligned16(zp, err);
-    }
-    if (ok) {
-        const uint4 ov = *reinterpret_cast<const uint4*>(op);
-        const uint4 gv = *reinterpret_cast<const uint4*>(gp);
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+    IDX prow = (IDX)blockIdx.x * RPB + threadIdx.x / G;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 of = __bfloat1622float2(o2[i]);
-            const float2 gf = __bfloat1622float2(g2[i]);
-            sum = fmaf(of.x, gf.x, sum);
-            sum = fmaf(of.y, gf.y, sum);
+    for (int k = 0; k < kRowsPerThread; ++k, prow += step) {
+        const IDX n = prow % n_pad;
+        const IDX bh = prow / n_pad;
+        float sum = 0.f;
+        bool ok = prow < rows && n < (IDX)a.N;
+        const __nv_bfloat16 *op = nullptr, *gp = nullptr;
+        float* zp = nullptr;
+        if (ok) {
+            const int h = (int)(bh % (IDX)a.H);
+            const int b = (int)(bh / (IDX)a.H);
+            op = row_ptr<__nv_bfloat16>(a.o, b, h, (long long)n) + part * 8;
+            gp = row_ptr<__nv_bfloat16>(a.dout, b, h, (long long)n) + part * 8;
+            zp = dq_acc + ((long long)bh * a.N + (long long)n) * D + part * 8;
+            ok = aligned16(op, err) && aligned16(gp, err) && aligned16(zp, err);
         }
-        float4* z = reinterpret_cast<float4*>(zp);
-        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+        if (ok) {
+            const uint4 ov = *reinterpret_cast<const uint4*>(op);
+            const uint4 gv = *reinterpret_cast<const uint4*>(gp);
+            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o, G);
-    if (prow < rows && part == 0) {
-        float nl = -INFINITY, dd = 0.f;
-        if (n < a.N) {
-            const float l = a.lse[bh * a.N + n];
-            nl = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
-            dd = -sum;
+            for (int i = 0; i < 4; ++i) {
+                const float2 of = __bfloat1622float2(o2[i]);
+                const float2 gf = __bfloat1622float2(g2[i]);
+                sum = fmaf(of.x, gf.x, sum);
+                sum = fmaf(of.y, gf.y, sum);
+            }
+            float4* z = reinterpret_cast<float4*>(zp);
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float* tile = stats + (bh * (n_pad / 128) + n / 128) * 256;
-        tile[n % 128] = nl;
-        tile[128 + n % 128] = dd;
+#pragma unroll
+        for (int o = G / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o, G);
+        if (prow < rows && part == 0) {
+            float nl = -INFINITY, dd = 0.f;
+            if (n < (IDX)a.N) {
+                const float l = a.lse[(long long)bh * a.N + (long long)n];
+                nl = (l == -INFINITY) ? -INFINITY : -l * kLog2e;
+                dd = -sum;
+            }
+            float* tile = stats + ((long long)bh * (n_pad / 128) + n / 128) * 256;
+            tile[n % 128] = nl;
+            tile[128 + n % 128] = dd;
+        }
     }
 }
 
 // ------------------------------------------------------------ dQ finalize
-template <int D>
+template <int D, typename IDX>
 __global__ void __launch_bounds__(256) bwd_dq_finalize_kernel(SimtArgs a, const float* dq_acc, int* err) {
     constexpr int G = D / 8;
-    const long long rows = (long long)a.B * a.H * a.N;
-    const long long row = (long long)blockIdx.x * (256 / G) + threadIdx.x / G;
+    constexpr int RPB = 256 / G;
+    const IDX rows = (IDX)a.B * (IDX)a.H * (IDX)a.N;
+    const IDX step = (IDX)gridDim.x * RPB;
     const int part = threadIdx.x % G;
-    if (row >= rows) return;
-    const int n = (int)(row % a.N);
-    const int h = (int)((row / a.N) % a.H);
-    const int b = (int)(row / ((long long)a.N * a.H));
-    const float4* src = reinterpret_cast<const float4*>(dq_acc + row * D + part * 8);
-    uint4* dst = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(row_ptr<__nv_bfloat16>(a.dq, b, h, n))) + part;
-    if (!aligned16(src, err) || !aligned16(dst, err)) return;
-    const float4 x = src[0], y = src[1];
-    uint4 out;
-    out.x = ptx::pack_bf16(x.x, x.y);
-    out.y = ptx::pack_bf16(x.z, x.w);
-    out.z = ptx::pack_bf16(y.x, y.y);
-    out.w = ptx::pack_bf16(y.z, y.w);
-    *dst = out;
+    IDX row = (IDX)blockIdx.x * RPB + threadIdx.x / G;
+    float4 x[kRowsPerThread], y[kRowsPerThread];
+    uint4* dst[kRowsPerThread];
+    // all loads first, then all stores
+#pragma unroll
+    for (int k = 0; k < kRowsPerThread; ++k, row += step) {
+        dst[k] = nullptr;
+        if (row >= rows) continue;
+        const IDX n = row % (IDX)a.N;
+        const IDX bhr = row / (IDX)a.N;
+        const int h = (int)(bhr % (IDX)a.H);
+        const int b = (int)(bhr / (IDX)a.H);
+        const float4* src = reinterpret_cast<const float4*>(dq_acc + (long long)row * D + part * 8);
+        uint4* d = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(row_ptr<__nv_bfloat16>(a.dq, b, h, (long long)n))) +
+                   part;
+        if (!aligned16(src, err) || !aligned16(d, err)) continue;
+        x[k] = src[0];
+        y[k] = src[1];
+        dst[k] = d;
+    }
+#pragma unroll
+    for (int k = 0; k < kRowsPerThread; ++k) {
+        if (dst[k] == nullptr) continue;
+        uint4 out;
+        out.x = ptx::pack_bf16(x[k].x, x[k].y);
+        out.y = ptx::pack_bf16(x[k].z, x[k].w);
+        out.z = ptx::pack_bf16(y[k].x, y[k].y);
+        out.w = ptx::pack_bf16(y[k].z, y[k].w);
+        *dst[k] = out;
+    }
 }
 
 Tensor4 tensor4(const void* p, const int64_t* s) { return Tensor4{p, (long long)s[0], (long long)s[1], (long long)s[2]}; }
@@ -292,27 +320,52 @@ cudaError_t launch_fwd_simt(const attn_fwd_params& p, cudaStream_t s) {
     return p.d == 64 ? fwd_simt_launch<float, 64>(a, s) : fwd_simt_launch<float, 128>(a, s);
 }
 
+namespace {
+// blocks for `rows` rows, kRowsPerThread rows per thread; 32-bit indexing if every
+// row index (plus one grid step of slack) fits
+struct RowGrid {
+    unsigned blocks;
+    bool idx32;
+};
+RowGrid row_grid(long long rows, int d) {
+    const long long rpb = 256 / (d / 8);
+    const long long per_block = rpb * kRowsPerThread;
+    const long long blocks = (rows + per_block - 1) / per_block;
+    return RowGrid{(unsigned)blocks, rows + blocks * rpb < (1ll << 31)};
+}
+template <int D>
+void prepass_t(const RowGrid& g, const SimtArgs& a, const BwdWorkspace& ws, int* err, cudaStream_t s) {
+    if (g.idx32)
+        bwd_prepass_kernel<D, unsigned><<<g.blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
+    else
+        bwd_prepass_kernel<D, unsigned long long><<<g.blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
+}
+template <int D>
+void finalize_t(const RowGrid& g, const SimtArgs& a, const BwdWorkspace& ws, int* err, cudaStream_t s) {
+    if (g.idx32)
+        bwd_dq_finalize_kernel<D, unsigned><<<g.blocks, 256, 0, s>>>(a, ws.dq_acc, err);
+    else
+        bwd_dq_finalize_kernel<D, unsigned long long><<<g.blocks, 256, 0, s>>>(a, ws.dq_acc, err);
+}
+}  // namespace
+
 cudaError_t launch_bwd_prepass(const attn_bwd_params& p, const BwdWorkspace& ws, int* err, cudaStream_t s) {
     const SimtArgs a = make_bwd_args(p, ws);
-    const long long rows = (long long)p.fwd.B * p.fwd.H * ((p.fwd.N + 127) / 128 * 128);
-    const int rows_per_block = 256 / (p.fwd.d / 8);
-    const unsigned blocks = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
+    const RowGrid g = row_grid((long long)p.fwd.B * p.fwd.H * ((p.fwd.N + 127) / 128 * 128), p.fwd.d);
     if (p.fwd.d == 64)
-        bwd_prepass_kernel<64><<<blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
+        prepass_t<64>(g, a, ws, err, s);
     else
-        bwd_prepass_kernel<128><<<blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
+        prepass_t<128>(g, a, ws, err, s);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_finalize(const attn_bwd_params& p, const BwdWorkspace& ws, int* err, cudaStream_t s) {
     const SimtArgs a = make_bwd_args(p, ws);
-    const long long rows = (long long)p.fwd.B * p.fwd.H * p.fwd.N;
-    const int rows_per_block = 256 / (p.fwd.d / 8);
-    const unsigned blocks = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
+    const RowGrid g = row_grid((long long)p.fwd.B * p.fwd.H * p.fwd.N, p.fwd.d);
     if (p.fwd.d == 64)
-        bwd_dq_finalize_kernel<64><<<blocks, 256, 0, s>>>(a, ws.dq_acc, err);
+        finalize_t<64>(g, a, ws, err, s);
     else
-        bwd_dq_finalize_kernel<128><<<blocks, 256, 0, s>>>(a, ws.dq_acc, err);
+        finalize_t<128>(g, a, ws, err, s);
     return cudaGetLastError();
 }
 
