@@ -436,8 +436,10 @@ __global__ void __launch_bounds__(384, 1)
 // stores.
 //
 // Warps (16): 0-7 P^T / dS^T (two warpgroups, 32 queries of each half each),
-// 8 TMA producer, 9 and 10 MMA issuers, 11 idle, 12-15 dQ drain. The drain has its
-// own warpgroup so the P^T / dS^T warps move on to the next half at once.
+// 8 TMA producer, 9 and 10 MMA issuers, 11 idle, 12-15 dQ drain and the
+// units' dV / dK epilogues. The drain and the epilogues have their own
+// warpgroup so the P^T / dS^T warps move on to the next half, and the next
+// unit, at once.
 // ============================================================================
 template <bool MASK>
 struct Bwd64Cfg {
@@ -463,7 +465,7 @@ struct Bwd64Cfg {
 struct __align__(8) Bwd64Barriers {
     uint64_t kv_full[2];              // per K/V buffer
     uint64_t kv_free[2];              // per K/V buffer: both issuers done with its unit's K and V
-    uint64_t dkv_empty;               // the warpgroups have read this unit's dV and dK
+    uint64_t dkv_empty;               // the drain warpgroup has read this unit's dV and dK
     uint64_t epi_staged, epi_free;    // dV / dK tile staged in shared memory / TMA store done reading it
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full[3], ds_ready[3];  // per S slot
@@ -532,8 +534,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&bar.kv_full[i], 1);
             mbar_init(&bar.kv_free[i], 2);
         }
-        mbar_init(&bar.dkv_empty, 256);
-        mbar_init(&bar.epi_staged, 256);
+        mbar_init(&bar.dkv_empty, 128);
+        mbar_init(&bar.epi_staged, 128);
         mbar_init(&bar.epi_free, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.st_full[i], 1);
@@ -737,7 +739,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         __syncwarp();
     } else if (warp < 8) {
-        // ------------------------------------------------ P^T, dS^T (thread = key row), dV / dK out
+        // ------------------------------------------------ P^T, dS^T (thread = key row)
         const int g = warp >> 2;  // this warpgroup's 32 queries of each half
         const int kr = (warp & 3) * 32 + lane;
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -830,6 +832,11 @@ __global__ void __launch_bounds__(512, 1)
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
+                if (hl == 0 && n > 0) {  // the previous unit's dV / dK stores have read this dS buffer
+                    ok = mbar_wait(&bar.epi_free, (n - 1) & 1, wc);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
                 // dS row kr, queries ql0 .. ql0+31 of tile buffer (gt & 1): box hf, chunks 4g .. 4g+3
                 uint8_t* box = smem + Cfg::kDSOff + (gt & 1) * Cfg::kDSBytes + hf * (128 * 128) + kr * 128;
 #pragma unroll
@@ -843,55 +850,12 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_before();
                 mbar_arrive(&bar.ds_ready[gu % 3]);
             }
-            if (!ok) break;
-            // unit epilogue: warpgroup 0 stages the dV rows, warpgroup 1 the scale * dK rows of
-            // this key tile in shared memory, and one thread stores both tiles with TMA
-            // (per-thread row stores would write 16 bytes to each of 32 rows per instruction).
-            // The staging area is the dS buffer of the unit's second-to-last tile, whose dQ
-            // product has read it; the next tile to write that buffer is this unit's successor's
-            // first, after the stores have read it (epi_free).
-            ok = mbar_wait(&bar.kv_done, n & 1, wc);
-            const int gl = gu / 2 - 1;  // this unit's last tile
-            if (gl >= 1) ok = ok && mbar_wait(&bar.dq_done[(gl - 1) & 1], ((gl - 1) >> 1) & 1, wc);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t v[64];
-            tmem_ld32_at<0>(tRow + 256 + g * D, v);
-            tmem_ld32_at<32>(tRow + 256 + g * D + 32, v);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bar.dkv_empty);  // the accumulators may take the next unit
-            const float mul = g == 0 ? 1.f : p.scale;
-            uint8_t* epi = smem + Cfg::kDSOff + ((gl + 1) & 1) * Cfg::kDSBytes + g * (128 * 128) + kr * 128;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(epi + ((c ^ (kr & 7)) << 4)) = make_uint4(
-                    pack_bf16(__uint_as_float(v[8 * c + 0]) * mul, __uint_as_float(v[8 * c + 1]) * mul),
-                    pack_bf16(__uint_as_float(v[8 * c + 2]) * mul, __uint_as_float(v[8 * c + 3]) * mul),
-                    pack_bf16(__uint_as_float(v[8 * c + 4]) * mul, __uint_as_float(v[8 * c + 5]) * mul),
-                    pack_bf16(__uint_as_float(v[8 * c + 6]) * mul, __uint_as_float(v[8 * c + 7]) * mul));
-            fence_proxy_async_smem();
-            mbar_arrive(&bar.epi_staged);
-            if (threadIdx.x == 0) {  // rows beyond N are clipped by the tensor maps
-                ok = mbar_wait(&bar.epi_staged, n & 1, wc);
-                if (ok) {
-                    const uint8_t* stg0 = smem + Cfg::kDSOff + ((gl + 1) & 1) * Cfg::kDSBytes;
-                    tma_store_4d(&tm_dv, stg0, 0, w.k0, w.h, w.b);
-                    tma_store_4d(&tm_dk, stg0 + 128 * 128, 0, w.k0, w.h, w.b);
-                    bulk_commit();
-                    bulk_wait_read0();
-                    mbar_arrive(&bar.epi_free);
-                }
-            }
-            ok = mbar_wait(&bar.epi_free, n & 1, wc);
-            ok = __all_sync(0xffffffffu, ok);
         }
-        if (threadIdx.x == 0) bulk_wait0();  // the dV / dK stores complete before the CTA exits
     }
 
     else if (warp >= 12) {
-        // ------------------------------------------------ dQ drain (thread = query row of the tile)
+        // ------------------------------------------------ dQ drain (thread = query row of the tile),
+        // then each unit's dV / dK epilogue
         // scale * dQ goes to shared memory in the 128-byte-swizzled layout of the
         // accumulator's tensor map (box bx = columns 32 bx .. 32 bx + 31), and one
         // thread adds both boxes into the fp32 accumulator with TMA reductions.
@@ -902,8 +866,8 @@ __global__ void __launch_bounds__(512, 1)
         const bool issuer = threadIdx.x == 384;
         if (issuer) prefetch_tmap(&tm_dq);
         bool ok = true;
-        int gt = 0;
-        for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku)) {
+        int gt = 0, n = 0;
+        for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku), ++n) {
             const Unit64 w = unit64(p, u);
             for (int it = 0; it < w.n_it && ok; ++it, ++gt) {
                 ok = mbar_wait(&bar.dq_full, gt & 1, wc);
@@ -948,8 +912,57 @@ __global__ void __launch_bounds__(512, 1)
                     }
                 }
             }
+            if (!ok) break;
+            // unit epilogue (thread = key row): dV and scale * dK leave through shared memory
+            // and TMA stores, so the P^T / dS^T warps go straight on to the next unit. The
+            // staging area is the dS buffer of the unit's second-to-last tile, which its dQ
+            // product has read; the next tile to write that buffer is the next unit's first,
+            // after these stores have read it (epi_free). Rows beyond N are clipped by the maps.
+            const int gl = gt - 1;  // this unit's last tile
+            ok = mbar_wait(&bar.kv_done, n & 1, wc);
+            if (gl >= 1) ok = ok && mbar_wait(&bar.dq_done[(gl - 1) & 1], ((gl - 1) >> 1) & 1, wc);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t kv[64];
+            tmem_ld32_at<0>(tRow + 256, kv);   // dV
+            tmem_ld32_at<32>(tRow + 288, kv);
+            tmem_wait_ld();
+            uint8_t* epi = smem + Cfg::kDSOff + ((gl + 1) & 1) * Cfg::kDSBytes;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(epi + qr * 128 + ((c ^ (qr & 7)) << 4)) =
+                    make_uint4(pack_bf16(__uint_as_float(kv[8 * c + 0]), __uint_as_float(kv[8 * c + 1])),
+                               pack_bf16(__uint_as_float(kv[8 * c + 2]), __uint_as_float(kv[8 * c + 3])),
+                               pack_bf16(__uint_as_float(kv[8 * c + 4]), __uint_as_float(kv[8 * c + 5])),
+                               pack_bf16(__uint_as_float(kv[8 * c + 6]), __uint_as_float(kv[8 * c + 7])));
+            tmem_ld32_at<0>(tRow + 320, kv);   // dK
+            tmem_ld32_at<32>(tRow + 352, kv);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&bar.dkv_empty);  // the accumulators may take the next unit
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(epi + 128 * 128 + qr * 128 + ((c ^ (qr & 7)) << 4)) = make_uint4(
+                    pack_bf16(__uint_as_float(kv[8 * c + 0]) * p.scale, __uint_as_float(kv[8 * c + 1]) * p.scale),
+                    pack_bf16(__uint_as_float(kv[8 * c + 2]) * p.scale, __uint_as_float(kv[8 * c + 3]) * p.scale),
+                    pack_bf16(__uint_as_float(kv[8 * c + 4]) * p.scale, __uint_as_float(kv[8 * c + 5]) * p.scale),
+                    pack_bf16(__uint_as_float(kv[8 * c + 6]) * p.scale, __uint_as_float(kv[8 * c + 7]) * p.scale));
+            fence_proxy_async_smem();
+            mbar_arrive(&bar.epi_staged);
+            if (issuer) {
+                ok = mbar_wait(&bar.epi_staged, n & 1, wc);
+                if (ok) {
+                    tma_store_4d(&tm_dv, epi, 0, w.k0, w.h, w.b);
+                    tma_store_4d(&tm_dk, epi + 128 * 128, 0, w.k0, w.h, w.b);
+                    bulk_commit();
+                    bulk_wait_read0();
+                    mbar_arrive(&bar.epi_free);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok);
         }
-        if (issuer) bulk_wait0();  // reductions complete before the CTA exits
+        if (issuer) bulk_wait0();  // reductions and stores complete before the CTA exits
     }
 
     tc_fence_before();

@@ -121,6 +121,18 @@ def test_fp32_edge_lengths(A, d):
             _check_fwd(o, lse, inp, causal, 0.1, f32=True)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_several_units_per_cta(A, causal):
+    # 2 x 12 heads x 8 key tiles = 192 units: more than one CTA per SM's worth, so
+    # persistent CTAs carry barrier phases, buffers and accumulators across units
+    B, H, N, d = 2, 12, 1024, 64
+    inp = {n: W.random_tensor((B, H, N, d), 800 + i, torch.bfloat16) for i, n in enumerate(("q", "k", "v", "do"))}
+    scale = 1 / math.sqrt(d)
+    o, lse = _run_fwd(A, inp, causal, scale)
+    _check_fwd(o, lse, inp, causal, scale)
+    _check_bwd(_run_bwd(A, inp, causal, scale, o, lse), inp, causal, scale)
+
+
 def test_bnhd_strided_layout(A):
     B, H, N, d = 2, 3, 333, 128
     base = {n: W.random_tensor((B, N, H, d), 300 + i, torch.bfloat16) for i, n in enumerate(("q", "k", "v", "do"))}
