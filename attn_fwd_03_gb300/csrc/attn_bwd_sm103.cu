@@ -94,6 +94,7 @@ struct __align__(8) BwdBarriers {
     uint64_t kv_full;
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full, ds_ready, dq_full, dq_empty, kv_done;
+    uint64_t dq_staged[2];  // per stage: the dQ tile staged in it for the TMA reduction
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -132,6 +133,11 @@ __global__ void __launch_bounds__(384, 1)
                   const __grid_constant__ CUtensorMap tm_dv,
                   const BwdParamsDev p) {
     using Cfg = BwdCfg<D, MASK>;
+    // dQ leaves through the current stage's Q/dO area and TMA reductions when there are
+    // two stages (the next tile's operands sit in the other); with one stage the staging
+    // would hold up the next tile's load, so the warpgroups reduce from registers.
+    constexpr bool kTmaDq = Cfg::kStages > 1;
+    static_assert(!kTmaDq || 2 * Cfg::kTileBytes >= BQ * D * 4, "dQ staging fits in a stage");
     extern __shared__ __align__(1024) uint8_t smem[];
     BwdBarriers& bar = *reinterpret_cast<BwdBarriers*>(smem + Cfg::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -155,7 +161,10 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(&bar.kv_full, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar.st_full[s], 1);
-            mbar_init(&bar.st_empty[s], 1);
+            // with two stages a stage is also the dQ staging area: free after the tile's MMAs
+            // and after the TMA reduction has read the staged dQ
+            mbar_init(&bar.st_empty[s], kTmaDq ? 2 : 1);
+            mbar_init(&bar.dq_staged[s], 256);
         }
         mbar_init(&bar.s_full, 1);
         mbar_init(&bar.ds_ready, 256);
@@ -277,6 +286,29 @@ __global__ void __launch_bounds__(384, 1)
             drain_wait(&bar.drain, 0, p.timeout_ns);
         }
         __syncwarp();
+    } else if (kTmaDq && warp == 10) {
+        // ------------------------------------------------ dQ reductions
+        // Once both warpgroups have staged their halves of a dQ tile (fp32, in the
+        // accumulator map's 32-column boxes with the 128-byte swizzle) in the tile's
+        // stage, one lane adds the four boxes into the accumulator with TMA and then
+        // releases the stage. Rows beyond N are clipped by the tensor map.
+        if (lane == 0) {
+            prefetch_tmap(&tm_dq);
+            bool ok = true;
+            for (int it = 0; it < n_it && ok; ++it) {
+                const int s = it % Cfg::kStages;
+                ok = mbar_wait(&bar.dq_staged[s], (it / Cfg::kStages) & 1, wc);
+                if (!ok) break;
+                const uint8_t* stg = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+                const int q0 = (i_begin + it) * BQ;
+#pragma unroll
+                for (int bx = 0; bx < D / 32; ++bx) tma_reduce_add_4d(&tm_dq, stg + bx * (BQ * 128), 32 * bx, q0, h, b);
+                bulk_commit();
+                bulk_wait_read0();
+                mbar_arrive(&bar.st_empty[s]);
+            }
+            bulk_wait0();  // reductions complete before the CTA exits
+        }
     } else if (warp < 8) {
         // ------------------------------------------------ P^T, dS^T, then the dQ drain
         // Two warpgroups share each query tile: warpgroup g takes query columns
@@ -365,7 +397,26 @@ __global__ void __launch_bounds__(384, 1)
             tc_fence_before();
             mbar_arrive(&bar.dq_empty);
             const int qg = q0 + kr;  // lane = query row of the dQ tile
-            if (qg < p.N) {
+            if constexpr (kTmaDq) {
+                // scale * dQ into this tile's stage: box (kDqCols / 32) g + bx holds columns
+                // 32 bx .. 32 bx + 31 of this warpgroup's half, 128 bytes per query row
+                uint8_t* stg = smem + Cfg::kStageOff + s * Cfg::kStageBytes + g * (kDqCols / 32) * (BQ * 128);
+#pragma unroll
+                for (int bx = 0; bx < kDqCols / 32; ++bx) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int col = 32 * bx + 4 * c;
+                        const float2 a0 = fmul2(make_float2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])),
+                                                make_float2(p.scale, p.scale));
+                        const float2 a1 = fmul2(make_float2(__uint_as_float(v[col + 2]), __uint_as_float(v[col + 3])),
+                                                make_float2(p.scale, p.scale));
+                        *reinterpret_cast<float4*>(stg + bx * (BQ * 128) + kr * 128 + ((c ^ (kr & 7)) << 4)) =
+                            make_float4(a0.x, a0.y, a1.x, a1.y);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bar.dq_staged[s]);
+            } else if (qg < p.N) {
                 float* dst = p.dq_acc + (((long long)b * p.H + h) * p.N + qg) * D + g * kDqCols;
 #pragma unroll
                 for (int c = 0; c < kDqCols; c += 4) {
