@@ -62,12 +62,14 @@ struct BwdCfg {
     static constexpr int kStages = (D == 128 && MASK) ? 1 : 2;
     static constexpr int kVecOffInStage = 2 * kTileBytes + (MASK ? kMaskBytes : 0);
     static constexpr int kStageBytes = kVecOffInStage + 1024;  // + [-LSE*log2e | D] x 128
-    static constexpr int kThreads = 384;
     static constexpr int kKOff = 0;
     static constexpr int kVOff = kKOff + kTileBytes;
     static constexpr int kDSOff = kVOff + kTileBytes;
     static constexpr int kStageOff = kDSOff + BQ * BK * 2;
-    static constexpr int kBarOff = kStageOff + kStages * kStageBytes;
+    // one stage: a separate area that holds half a dQ tile (one warpgroup's columns) at a time
+    static constexpr int kStgOff = kStageOff + kStages * kStageBytes;
+    static constexpr int kStgBytes = kStages == 1 ? BQ * (D / 2) * 4 : 0;
+    static constexpr int kBarOff = kStgOff + kStgBytes;
     static constexpr int kSmemBytes = kBarOff + 256;
     static constexpr uint32_t kIdescS = idesc_bf16(BK, BQ, false, false);   // S^T, dP^T
     static constexpr uint32_t kIdescKV = idesc_bf16(BK, D, false, true);    // dV, dK (A in TMEM)
@@ -94,7 +96,9 @@ struct __align__(8) BwdBarriers {
     uint64_t kv_full;
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full, ds_ready, dq_full, dq_empty, kv_done;
-    uint64_t dq_staged[2];  // per stage: the dQ tile staged in it for the TMA reduction
+    uint64_t dq_staged[2];  // two stages: per stage, the dQ tile staged in it for the TMA reduction;
+                            // one stage: [0] a warpgroup's half staged in the separate area
+    uint64_t stg_free;      // one stage: the separate area read by the last reduction
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -120,10 +124,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
     while (!mbar_try_wait(a, parity))
         if (globaltimer() - t0 > timeout_ns) break;
 }
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
 
 template <int D, bool MASK>
 __global__ void __launch_bounds__(384, 1)
@@ -133,11 +133,12 @@ __global__ void __launch_bounds__(384, 1)
                   const __grid_constant__ CUtensorMap tm_dv,
                   const BwdParamsDev p) {
     using Cfg = BwdCfg<D, MASK>;
-    // dQ leaves through the current stage's Q/dO area and TMA reductions when there are
-    // two stages (the next tile's operands sit in the other); with one stage the staging
-    // would hold up the next tile's load, so the warpgroups reduce from registers.
-    constexpr bool kTmaDq = Cfg::kStages > 1;
-    static_assert(!kTmaDq || 2 * Cfg::kTileBytes >= BQ * D * 4, "dQ staging fits in a stage");
+    // dQ leaves through shared memory and TMA reductions. With two stages the current
+    // stage's Q/dO area holds the whole tile (the next tile's operands sit in the other
+    // stage); with one stage, staging there would hold up the next tile's load, so the
+    // two warpgroups take turns with a separate half-tile area.
+    constexpr bool kStageDq = Cfg::kStages > 1;
+    static_assert(!kStageDq || 2 * Cfg::kTileBytes >= BQ * D * 4, "dQ staging fits in a stage");
     extern __shared__ __align__(1024) uint8_t smem[];
     BwdBarriers& bar = *reinterpret_cast<BwdBarriers*>(smem + Cfg::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -163,9 +164,10 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&bar.st_full[s], 1);
             // with two stages a stage is also the dQ staging area: free after the tile's MMAs
             // and after the TMA reduction has read the staged dQ
-            mbar_init(&bar.st_empty[s], kTmaDq ? 2 : 1);
-            mbar_init(&bar.dq_staged[s], 256);
+            mbar_init(&bar.st_empty[s], kStageDq ? 2 : 1);
+            mbar_init(&bar.dq_staged[s], kStageDq ? 256 : 128);
         }
+        mbar_init(&bar.stg_free, 1);
         mbar_init(&bar.s_full, 1);
         mbar_init(&bar.ds_ready, 256);
         mbar_init(&bar.dq_full, 1);
@@ -286,26 +288,42 @@ __global__ void __launch_bounds__(384, 1)
             drain_wait(&bar.drain, 0, p.timeout_ns);
         }
         __syncwarp();
-    } else if (kTmaDq && warp == 10) {
+    } else if (warp == 10) {
         // ------------------------------------------------ dQ reductions
-        // Once both warpgroups have staged their halves of a dQ tile (fp32, in the
-        // accumulator map's 32-column boxes with the 128-byte swizzle) in the tile's
-        // stage, one lane adds the four boxes into the accumulator with TMA and then
-        // releases the stage. Rows beyond N are clipped by the tensor map.
+        // Once a dQ tile (two stages) or one warpgroup's half of it (one stage) is
+        // staged (fp32, in the accumulator map's 32-column boxes with the 128-byte
+        // swizzle), one lane adds the boxes into the accumulator with TMA and frees
+        // the staging area: the tile's stage, or the separate area. Rows beyond N
+        // are clipped by the tensor map.
         if (lane == 0) {
             prefetch_tmap(&tm_dq);
             bool ok = true;
             for (int it = 0; it < n_it && ok; ++it) {
-                const int s = it % Cfg::kStages;
-                ok = mbar_wait(&bar.dq_staged[s], (it / Cfg::kStages) & 1, wc);
-                if (!ok) break;
-                const uint8_t* stg = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
                 const int q0 = (i_begin + it) * BQ;
+                if constexpr (kStageDq) {
+                    const int s = it % Cfg::kStages;
+                    ok = mbar_wait(&bar.dq_staged[s], (it / Cfg::kStages) & 1, wc);
+                    if (!ok) break;
+                    const uint8_t* stg = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
 #pragma unroll
-                for (int bx = 0; bx < D / 32; ++bx) tma_reduce_add_4d(&tm_dq, stg + bx * (BQ * 128), 32 * bx, q0, h, b);
-                bulk_commit();
-                bulk_wait_read0();
-                mbar_arrive(&bar.st_empty[s]);
+                    for (int bx = 0; bx < D / 32; ++bx)
+                        tma_reduce_add_4d(&tm_dq, stg + bx * (BQ * 128), 32 * bx, q0, h, b);
+                    bulk_commit();
+                    bulk_wait_read0();
+                    mbar_arrive(&bar.st_empty[s]);
+                } else {
+                    for (int g = 0; g < 2 && ok; ++g) {  // staging use k = 2 it + g
+                        ok = mbar_wait(&bar.dq_staged[0], g, wc);
+                        if (!ok) break;
+                        const uint8_t* stg = smem + Cfg::kStgOff;
+#pragma unroll
+                        for (int bx = 0; bx < D / 64; ++bx)
+                            tma_reduce_add_4d(&tm_dq, stg + bx * (BQ * 128), g * (D / 2) + 32 * bx, q0, h, b);
+                        bulk_commit();
+                        bulk_wait_read0();
+                        mbar_arrive(&bar.stg_free);
+                    }
+                }
             }
             bulk_wait0();  // reductions complete before the CTA exits
         }
@@ -396,37 +414,36 @@ __global__ void __launch_bounds__(384, 1)
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&bar.dq_empty);
-            const int qg = q0 + kr;  // lane = query row of the dQ tile
-            if constexpr (kTmaDq) {
-                // scale * dQ into this tile's stage: box (kDqCols / 32) g + bx holds columns
-                // 32 bx .. 32 bx + 31 of this warpgroup's half, 128 bytes per query row
-                uint8_t* stg = smem + Cfg::kStageOff + s * Cfg::kStageBytes + g * (kDqCols / 32) * (BQ * 128);
-#pragma unroll
-                for (int bx = 0; bx < kDqCols / 32; ++bx) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const int col = 32 * bx + 4 * c;
-                        const float2 a0 = fmul2(make_float2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])),
-                                                make_float2(p.scale, p.scale));
-                        const float2 a1 = fmul2(make_float2(__uint_as_float(v[col + 2]), __uint_as_float(v[col + 3])),
-                                                make_float2(p.scale, p.scale));
-                        *reinterpret_cast<float4*>(stg + bx * (BQ * 128) + kr * 128 + ((c ^ (kr & 7)) << 4)) =
-                            make_float4(a0.x, a0.y, a1.x, a1.y);
-                    }
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&bar.dq_staged[s]);
-            } else if (qg < p.N) {
-                float* dst = p.dq_acc + (((long long)b * p.H + h) * p.N + qg) * D + g * kDqCols;
-#pragma unroll
-                for (int c = 0; c < kDqCols; c += 4) {
-                    const float2 a0 = fmul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
-                                            make_float2(p.scale, p.scale));
-                    const float2 a1 = fmul2(make_float2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])),
-                                            make_float2(p.scale, p.scale));
-                    red_add_v4(dst + c, a0.x, a0.y, a1.x, a1.y);
+            // scale * dQ into the staging area: box bx (32 columns, 128 bytes per query row)
+            // of this warpgroup's half. Two stages: this tile's stage holds both halves;
+            // one stage: the separate area holds one half, warpgroup 0's first.
+            uint8_t* stg;
+            if constexpr (kStageDq) {
+                stg = smem + Cfg::kStageOff + s * Cfg::kStageBytes + g * (kDqCols / 32) * (BQ * 128);
+            } else {
+                stg = smem + Cfg::kStgOff;
+                const int k = 2 * it + g;  // staging use; wait for use k-1 to have been read
+                if (k > 0) {
+                    ok = mbar_wait(&bar.stg_free, (k - 1) & 1, wc);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
                 }
             }
+#pragma unroll
+            for (int bx = 0; bx < kDqCols / 32; ++bx) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int col = 32 * bx + 4 * c;
+                    const float2 a0 = fmul2(make_float2(__uint_as_float(v[col]), __uint_as_float(v[col + 1])),
+                                            make_float2(p.scale, p.scale));
+                    const float2 a1 = fmul2(make_float2(__uint_as_float(v[col + 2]), __uint_as_float(v[col + 3])),
+                                            make_float2(p.scale, p.scale));
+                    *reinterpret_cast<float4*>(stg + bx * (BQ * 128) + kr * 128 + ((c ^ (kr & 7)) << 4)) =
+                        make_float4(a0.x, a0.y, a1.x, a1.y);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bar.dq_staged[kStageDq ? s : 0]);
         }
         // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of this key tile
         if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
@@ -502,7 +519,6 @@ struct Bwd64Cfg {
     static constexpr int kStageBytes = kVecOffInStage + 1024;
     static constexpr int kDSBytes = BQ * BK * 2;  // one dS tile (two 64-query boxes)
     static constexpr int kKOff = 0;             // K, V of unit n in buffer n & 1: K at kKOff + 2 tiles x buffer
-    static constexpr int kVOff = kTileBytes;    // V right after its K
     static constexpr int kDSOff = 4 * kTileBytes;  // two dS buffers
     static constexpr int kStageOff = kDSOff + 2 * kDSBytes;
     static constexpr int kStgOff = kStageOff + kStages * kStageBytes;  // dQ staging: 2 boxes of 32 fp32 x 128 rows
