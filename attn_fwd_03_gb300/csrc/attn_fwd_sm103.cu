@@ -107,6 +107,7 @@ struct FwdParamsDev {
     long long o_sb, o_sh, o_sn;
     int mask_hb, mask_bb;  // 1 if the mask varies along h / b
     int num_units, n_qblk;
+    int head_major;        // unit order: heads outermost (see decode_unit)
     int* err;
     unsigned long long timeout_ns;
     int stall_after;
@@ -133,10 +134,18 @@ struct Unit {
 __device__ __forceinline__ Unit decode_unit(const FwdParamsDev& p, int u) {
     Unit w;
     const int bh = p.B * p.H;
-    // heaviest query blocks first (causal), heads innermost so neighbouring
-    // CTAs share K/V of the same batch and mask rows of the same block
-    w.qblk = p.n_qblk - 1 - u / bh;
-    const int r = u % bh;
+    int r;
+    if (p.head_major) {
+        // all units weigh the same (no causal mask): heads outermost, so the CTAs running
+        // at one time share the K/V of a few heads, which stay in L2
+        r = u / p.n_qblk;
+        w.qblk = u % p.n_qblk;
+    } else {
+        // heaviest query blocks first (causal), heads innermost so neighbouring CTAs
+        // share the mask rows of the same block
+        w.qblk = p.n_qblk - 1 - u / bh;
+        r = u % bh;
+    }
     w.b = r / p.H;
     w.h = r % p.H;
     const int nk_all = (p.N + BN - 1) / BN;
@@ -694,6 +703,7 @@ cudaError_t launch_tc(const attn_fwd_params& prm, const FwdMaps& maps, const Lau
     p.mask_hb = prm.mask ? (prm.mask_stride[1] != 0) : 0;
     p.mask_bb = prm.mask ? (prm.mask_stride[0] != 0) : 0;
     p.n_qblk = (prm.N + 2 * BM - 1) / (2 * BM);
+    p.head_major = !prm.causal && !MASK;
     p.num_units = p.n_qblk * prm.B * prm.H;
     p.err = lc.err;
     p.timeout_ns = lc.timeout_ns;
