@@ -26,6 +26,7 @@ ATTN_ERR_TIMEOUT = -5
 ATTN_ERR_WORKSPACE = -6
 ATTN_BF16 = 0
 ATTN_F32 = 1
+ATTN_F16 = 2
 
 STATUS_NAMES = {
     ATTN_OK: "ATTN_OK", ATTN_ERR_INVALID: "ATTN_ERR_INVALID", ATTN_ERR_UNSUPPORTED: "ATTN_ERR_UNSUPPORTED",
@@ -118,6 +119,8 @@ def _dtype_code(t: torch.dtype) -> int:
         return ATTN_BF16
     if t == torch.float32:
         return ATTN_F32
+    if t == torch.float16:
+        return ATTN_F16
     raise TypeError(f"unsupported dtype {t}")
 
 

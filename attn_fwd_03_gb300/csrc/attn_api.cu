@@ -100,7 +100,8 @@ attn_status_t check_fwd(const attn_fwd_params* p, bool* empty) {
     if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
     if (p->B < 0 || p->H < 0 || p->N < 0)
         return fail(ATTN_ERR_INVALID, "negative size B=%d H=%d N=%d", p->B, p->H, p->N);
-    if (p->dtype != ATTN_BF16 && p->dtype != ATTN_F32) return fail(ATTN_ERR_INVALID, "unknown dtype %d", p->dtype);
+    if (p->dtype != ATTN_BF16 && p->dtype != ATTN_F32 && p->dtype != ATTN_F16)
+        return fail(ATTN_ERR_INVALID, "unknown dtype %d", p->dtype);
     if (p->causal != 0 && p->causal != 1) return fail(ATTN_ERR_INVALID, "causal must be 0 or 1, got %d", p->causal);
     if (p->reserved0 != 0) return fail(ATTN_ERR_INVALID, "reserved0 must be 0");
     if (!std::isfinite(p->scale) || !(p->scale > 0.f))
@@ -136,10 +137,11 @@ attn_status_t get_encoder() {
     return ATTN_OK;
 }
 
-// 4-D bf16 map over (col, row, h, b) with a 64 x box_rows box and the 128-byte
-// swizzle: one box is box_rows rows of 128 bytes.
-attn_status_t encode_bf16_map(CUtensorMap* m, const char* name, const void* base, uint64_t cols, uint64_t rows,
-                              uint64_t hs, uint64_t bs, const int64_t* st, uint32_t box_rows) {
+// 4-D map of 16-bit elements (bf16 or fp16, as `dtype` says) over (col, row, h, b)
+// with a 64 x box_rows box and the 128-byte swizzle: one box is box_rows rows of
+// 128 bytes.
+attn_status_t encode_h16_map(CUtensorMap* m, const char* name, const void* base, uint64_t cols, uint64_t rows,
+                             uint64_t hs, uint64_t bs, const int64_t* st, uint32_t box_rows, int32_t dtype) {
     cuuint64_t dims[4] = {cols, rows, hs, bs};
     cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
     // a dimension of extent 1 may carry stride 0 (broadcast); give it a legal one
@@ -147,7 +149,9 @@ attn_status_t encode_bf16_map(CUtensorMap* m, const char* name, const void* base
         if (strides[i] == 0) strides[i] = 16;
     cuuint32_t box[4] = {64, box_rows, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+    const CUtensorMapDataType dt =
+        dtype == ATTN_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
@@ -175,14 +179,15 @@ attn_status_t build_fwd_maps(const attn_fwd_params& p, FwdMaps* m) {
     attn_status_t st = get_encoder();
     if (st != ATTN_OK) return st;
     const uint64_t N = (uint64_t)p.N, d = (uint64_t)p.d;
-    if ((st = encode_bf16_map(&m->q, "q", p.q, d, N, p.H, p.B, p.q_stride, 128)) != ATTN_OK) return st;
-    if ((st = encode_bf16_map(&m->k, "k", p.k, d, N, p.H, p.B, p.k_stride, 128)) != ATTN_OK) return st;
-    if ((st = encode_bf16_map(&m->v, "v", p.v, d, N, p.H, p.B, p.v_stride, 128)) != ATTN_OK) return st;
-    if ((st = encode_bf16_map(&m->o, "o", p.o, d, N, p.H, p.B, p.o_stride, 128)) != ATTN_OK) return st;
+    const int32_t DT = p.dtype;
+    if ((st = encode_h16_map(&m->q, "q", p.q, d, N, p.H, p.B, p.q_stride, 128, DT)) != ATTN_OK) return st;
+    if ((st = encode_h16_map(&m->k, "k", p.k, d, N, p.H, p.B, p.k_stride, 128, DT)) != ATTN_OK) return st;
+    if ((st = encode_h16_map(&m->v, "v", p.v, d, N, p.H, p.B, p.v_stride, 128, DT)) != ATTN_OK) return st;
+    if ((st = encode_h16_map(&m->o, "o", p.o, d, N, p.H, p.B, p.o_stride, 128, DT)) != ATTN_OK) return st;
     if (p.mask) {
         const uint64_t hm = p.mask_stride[1] != 0 ? (uint64_t)p.H : 1;
         const uint64_t bm = p.mask_stride[0] != 0 ? (uint64_t)p.B : 1;
-        if ((st = encode_bf16_map(&m->mask, "mask", p.mask, N, N, hm, bm, p.mask_stride, 128)) != ATTN_OK)
+        if ((st = encode_h16_map(&m->mask, "mask", p.mask, N, N, hm, bm, p.mask_stride, 128, DT)) != ATTN_OK)
             return st;
     } else {
         m->mask = m->q;  // unused by the kernel variant without a mask
@@ -199,9 +204,10 @@ attn_status_t build_bwd_maps(const attn_bwd_params& p, BwdMaps* m) {
     m->v = f.v;
     m->mask = f.mask;
     const uint64_t N = (uint64_t)p.fwd.N, d = (uint64_t)p.fwd.d;
-    if ((st = encode_bf16_map(&m->dk, "dk", p.dk, d, N, p.fwd.H, p.fwd.B, p.dk_stride, 128)) != ATTN_OK) return st;
-    if ((st = encode_bf16_map(&m->dv, "dv", p.dv, d, N, p.fwd.H, p.fwd.B, p.dv_stride, 128)) != ATTN_OK) return st;
-    return encode_bf16_map(&m->dout, "dout", p.dout, d, N, p.fwd.H, p.fwd.B, p.do_stride, 128);
+    const int32_t DT = p.fwd.dtype;
+    if ((st = encode_h16_map(&m->dk, "dk", p.dk, d, N, p.fwd.H, p.fwd.B, p.dk_stride, 128, DT)) != ATTN_OK) return st;
+    if ((st = encode_h16_map(&m->dv, "dv", p.dv, d, N, p.fwd.H, p.fwd.B, p.dv_stride, 128, DT)) != ATTN_OK) return st;
+    return encode_h16_map(&m->dout, "dout", p.dout, d, N, p.fwd.H, p.fwd.B, p.do_stride, 128, DT);
 }
 
 }  // namespace
@@ -235,7 +241,7 @@ attn_status_t bwd_check_inputs(const attn_bwd_params* p, bool* empty) {
     if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
     attn_status_t st = check_fwd(&p->fwd, empty);
     if (st != ATTN_OK) return st;
-    if (p->fwd.dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 only");
+    if (p->fwd.dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 and fp16 only");
     if (*empty) return ATTN_OK;
     if ((st = check_tensor("dout", p->dout, p->do_stride, 2, false)) != ATTN_OK) return st;
     if ((st = check_tensor("dq", p->dq, p->dq_stride, 2, false)) != ATTN_OK) return st;
@@ -303,7 +309,7 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
     bool empty = false;
     attn_status_t st = check_fwd(&p->fwd, &empty);
     if (st != ATTN_OK) return st;
-    if (p->fwd.dtype != ATTN_BF16) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 only");
+    if (p->fwd.dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 and fp16 only");
     if (empty) return ATTN_OK;
     if ((st = check_tensor("dout", p->dout, p->do_stride, 2, false)) != ATTN_OK) return st;
     if ((st = check_tensor("dq", p->dq, p->dq_stride, 2, false)) != ATTN_OK) return st;

@@ -71,9 +71,6 @@ struct BwdCfg {
     static constexpr int kStgBytes = kStages == 1 ? BQ * (D / 2) * 4 : 0;
     static constexpr int kBarOff = kStgOff + kStgBytes;
     static constexpr int kSmemBytes = kBarOff + 256;
-    static constexpr uint32_t kIdescS = idesc_bf16(BK, BQ, false, false);   // S^T, dP^T
-    static constexpr uint32_t kIdescKV = idesc_bf16(BK, D, false, true);    // dV, dK (A in TMEM)
-    static constexpr uint32_t kIdescQ = idesc_bf16(BQ, 64, true, true);     // dQ half (A = dS query-major)
 };
 
 struct BwdParamsDev {
@@ -125,7 +122,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
         if (globaltimer() - t0 > timeout_ns) break;
 }
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool F16>
 __global__ void __launch_bounds__(384, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -133,6 +130,10 @@ __global__ void __launch_bounds__(384, 1)
                   const __grid_constant__ CUtensorMap tm_dv,
                   const BwdParamsDev p) {
     using Cfg = BwdCfg<D, MASK>;
+    // 16-bit element type of the operands and of P^T, dS^T: bf16, or IEEE half when F16
+    constexpr uint32_t kIdescS = idesc_h16(BK, BQ, false, false, F16);  // S^T, dP^T
+    constexpr uint32_t kIdescKV = idesc_h16(BK, D, false, true, F16);   // dV, dK (A in TMEM)
+    constexpr uint32_t kIdescQ = idesc_h16(BQ, 64, true, true, F16);    // dQ half (A = dS query-major)
     // dQ leaves through shared memory and TMA reductions. With two stages the current
     // stage's Q/dO area holds the whole tile (the next tile's operands sit in the other
     // stage); with one stage, staging there would hold up the next tile's load, so the
@@ -252,10 +253,10 @@ __global__ void __launch_bounds__(384, 1)
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 0, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + 0, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+                    mma_ss(tmem + 128, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), kIdescS, kk > 0 ? 1u : 0u);
                 mma_commit(&bar.s_full);
             }
             __syncwarp();
@@ -265,18 +266,18 @@ __global__ void __launch_bounds__(384, 1)
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), Cfg::kIdescKV,
+                    mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), kIdescKV,
                            (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + 256 + D, tmem + 128 + packed_col_k(kk), mnmajor_desc(sQ, kk), Cfg::kIdescKV,
+                    mma_ts(tmem + 256 + D, tmem + 128 + packed_col_k(kk), mnmajor_desc(sQ, kk), kIdescKV,
                            (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int half = 0; half < D / 64; ++half)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         mma_ss(tmem + (half == 0 ? 64 : 192), mnmajor_desc(sDS, kk),
-                               mnmajor_desc(sK + half * 128 * 128, kk), Cfg::kIdescQ, kk > 0 ? 1u : 0u);
+                               mnmajor_desc(sK + half * 128 * 128, kk), kIdescQ, kk > 0 ? 1u : 0u);
                 mma_commit(&bar.dq_full);
                 mma_commit(&bar.st_empty[s]);
             }
@@ -373,9 +374,9 @@ __global__ void __launch_bounds__(384, 1)
                     float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl);
                     if (MASK) {
                         const int kb = kr >> 6, kc = (kr & 63) >> 3;
-                        const float m0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                        const float m0 = h16_to_float<F16>(*reinterpret_cast<const uint16_t*>(
                             mt + kb * 128 * 128 + q * 128 + ((kc ^ (q & 7)) << 4) + (kr & 7) * 2));
-                        const float m1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                        const float m1 = h16_to_float<F16>(*reinterpret_cast<const uint16_t*>(
                             mt + kb * 128 * 128 + (q + 1) * 128 + ((kc ^ ((q + 1) & 7)) << 4) + (kr & 7) * 2));
                         x = ffma2(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
                     }
@@ -384,8 +385,8 @@ __global__ void __launch_bounds__(384, 1)
                     const float2 pr = make_float2(ex2(x.x), ex2(x.y));
                     const float2 ds =
                         fmul2(pr, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd));
-                    pk[i / 2] = pack_bf16(pr.x, pr.y);
-                    dk[i / 2] = pack_bf16(ds.x, ds.y);
+                    pk[i / 2] = pack_h16<F16>(pr.x, pr.y);
+                    dk[i / 2] = pack_h16<F16>(ds.x, ds.y);
                 }
                 tmem_st16(tRow + packed_col(c), pk);
                 tmem_st16(tRow + 128 + packed_col(c), dk);
@@ -463,10 +464,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         dst[q] = make_uint4(
-                            pack_bf16(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
-                            pack_bf16(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
-                            pack_bf16(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
-                            pack_bf16(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+                            pack_h16<F16>(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                            pack_h16<F16>(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
+                            pack_h16<F16>(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
+                            pack_h16<F16>(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
                 }
             }
         }
@@ -524,9 +525,6 @@ struct Bwd64Cfg {
     static constexpr int kStgOff = kStageOff + kStages * kStageBytes;  // dQ staging: 2 boxes of 32 fp32 x 128 rows
     static constexpr int kBarOff = kStgOff + BQ * D * 4;
     static constexpr int kSmemBytes = kBarOff + 256;
-    static constexpr uint32_t kIdescS = idesc_bf16(BK, 64, false, false);  // S^T / dP^T of a half
-    static constexpr uint32_t kIdescKV = idesc_bf16(BK, D, false, true);   // dV, dK (A in TMEM)
-    static constexpr uint32_t kIdescQ = idesc_bf16(BQ, D, true, true);     // dQ (A = dS query-major)
 };
 
 struct __align__(8) Bwd64Barriers {
@@ -576,7 +574,7 @@ __device__ __forceinline__ int bwd_unit_at(int k) {
     return k * g + ((k & 1) ? g - 1 - i : i);
 }
 
-template <bool MASK>
+template <bool MASK, bool F16>
 __global__ void __launch_bounds__(512, 1)
     bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -585,6 +583,10 @@ __global__ void __launch_bounds__(512, 1)
                     const BwdParamsDev p) {
     using Cfg = Bwd64Cfg<MASK>;
     constexpr int D = 64;
+    // 16-bit element type of the operands and of P^T, dS^T: bf16, or IEEE half when F16
+    constexpr uint32_t kIdescS = idesc_h16(BK, 64, false, false, F16);  // S^T / dP^T of a half
+    constexpr uint32_t kIdescKV = idesc_h16(BK, D, false, true, F16);   // dV, dK (A in TMEM)
+    constexpr uint32_t kIdescQ = idesc_h16(BQ, D, true, true, F16);     // dQ (A = dS query-major)
     extern __shared__ __align__(1024) uint8_t smem[];
     Bwd64Barriers& bar = *reinterpret_cast<Bwd64Barriers*>(smem + Cfg::kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -739,11 +741,11 @@ __global__ void __launch_bounds__(512, 1)
                     if (elect_one()) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss(tmem + s_slot_col(gu), kmajor_desc(sK, kk), kmajor_desc(sQ, kk), Cfg::kIdescS,
+                            mma_ss(tmem + s_slot_col(gu), kmajor_desc(sK, kk), kmajor_desc(sQ, kk), kIdescS,
                                    kk > 0 ? 1u : 0u);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss(tmem + dp_slot_col(gu), kmajor_desc(sV, kk), kmajor_desc(sdO, kk), Cfg::kIdescS,
+                            mma_ss(tmem + dp_slot_col(gu), kmajor_desc(sV, kk), kmajor_desc(sdO, kk), kIdescS,
                                    kk > 0 ? 1u : 0u);
                         mma_commit(&bar.s_full[gu % 3]);
                     }
@@ -764,11 +766,11 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_ts(tmem + 256, tmem + s_slot_col(gu) + half_packed_col(kk), mnmajor_desc(sdO, kk),
-                                   Cfg::kIdescKV, (vl > 0 || kk > 0) ? 1u : 0u);
+                                   kIdescKV, (vl > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_ts(tmem + 320, tmem + s_slot_col(gu) + 16 + half_packed_col(kk),
-                                   mnmajor_desc(sQ, kk), Cfg::kIdescKV, (vl > 0 || kk > 0) ? 1u : 0u);
+                                   mnmajor_desc(sQ, kk), kIdescKV, (vl > 0 || kk > 0) ? 1u : 0u);
                         mma_commit(&bar.buf_free[gu % 3]);
                         // the tile's last reads of Q and dO (its scores completed before ds_ready)
                         if (hv == 1) mma_commit(&bar.st_empty[sv]);
@@ -785,7 +787,7 @@ __global__ void __launch_bounds__(512, 1)
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < BK / 16; ++kk)
-                                mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), Cfg::kIdescQ,
+                                mma_ss(tmem + 384, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), kIdescQ,
                                        kk > 0 ? 1u : 0u);
                             mma_commit(&bar.dq_full);
                             mma_commit(&bar.dq_done[gt & 1]);
@@ -862,10 +864,10 @@ __global__ void __launch_bounds__(512, 1)
                         const float2 d1 = fmul2(
                             p1, fadd2(make_float2(__uint_as_float(pv[i + 2]), __uint_as_float(pv[i + 3])),
                                       make_float2(nd.z, nd.w)));
-                        pk[i / 2] = pack_bf16(p0.x, p0.y);
-                        pk[i / 2 + 1] = pack_bf16(p1.x, p1.y);
-                        dk[i / 2] = pack_bf16(d0.x, d0.y);
-                        dk[i / 2 + 1] = pack_bf16(d1.x, d1.y);
+                        pk[i / 2] = pack_h16<F16>(p0.x, p0.y);
+                        pk[i / 2 + 1] = pack_h16<F16>(p1.x, p1.y);
+                        dk[i / 2] = pack_h16<F16>(d0.x, d0.y);
+                        dk[i / 2 + 1] = pack_h16<F16>(d1.x, d1.y);
                     }
                 } else {
 #pragma unroll
@@ -876,9 +878,9 @@ __global__ void __launch_bounds__(512, 1)
                         float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl);
                         if (MASK) {
                             const int kb = kr >> 6, kc = (kr & 63) >> 3;
-                            const float m0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                            const float m0 = h16_to_float<F16>(*reinterpret_cast<const uint16_t*>(
                                 mt + kb * 128 * 128 + q * 128 + ((kc ^ (q & 7)) << 4) + (kr & 7) * 2));
-                            const float m1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                            const float m1 = h16_to_float<F16>(*reinterpret_cast<const uint16_t*>(
                                 mt + kb * 128 * 128 + (q + 1) * 128 + ((kc ^ ((q + 1) & 7)) << 4) + (kr & 7) * 2));
                             x = ffma2(make_float2(m0, m1), make_float2(kLog2e, kLog2e), x);
                         }
@@ -887,8 +889,8 @@ __global__ void __launch_bounds__(512, 1)
                         const float2 pr = make_float2(ex2(x.x), ex2(x.y));
                         const float2 ds =
                             fmul2(pr, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd));
-                        pk[i / 2] = pack_bf16(pr.x, pr.y);
-                        dk[i / 2] = pack_bf16(ds.x, ds.y);
+                        pk[i / 2] = pack_h16<F16>(pr.x, pr.y);
+                        dk[i / 2] = pack_h16<F16>(ds.x, ds.y);
                     }
                 }
                 // P^T and dS^T pairs go into the 32 S^T columns this thread just read
@@ -999,10 +1001,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<uint4*>(epi + qr * 128 + ((c ^ (qr & 7)) << 4)) =
-                    make_uint4(pack_bf16(__uint_as_float(kv[8 * c + 0]), __uint_as_float(kv[8 * c + 1])),
-                               pack_bf16(__uint_as_float(kv[8 * c + 2]), __uint_as_float(kv[8 * c + 3])),
-                               pack_bf16(__uint_as_float(kv[8 * c + 4]), __uint_as_float(kv[8 * c + 5])),
-                               pack_bf16(__uint_as_float(kv[8 * c + 6]), __uint_as_float(kv[8 * c + 7])));
+                    make_uint4(pack_h16<F16>(__uint_as_float(kv[8 * c + 0]), __uint_as_float(kv[8 * c + 1])),
+                               pack_h16<F16>(__uint_as_float(kv[8 * c + 2]), __uint_as_float(kv[8 * c + 3])),
+                               pack_h16<F16>(__uint_as_float(kv[8 * c + 4]), __uint_as_float(kv[8 * c + 5])),
+                               pack_h16<F16>(__uint_as_float(kv[8 * c + 6]), __uint_as_float(kv[8 * c + 7])));
             tmem_ld32_at<0>(tRow + 320, kv);   // dK
             tmem_ld32_at<32>(tRow + 352, kv);
             tmem_wait_ld();
@@ -1011,10 +1013,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<uint4*>(epi + 128 * 128 + qr * 128 + ((c ^ (qr & 7)) << 4)) = make_uint4(
-                    pack_bf16(__uint_as_float(kv[8 * c + 0]) * p.scale, __uint_as_float(kv[8 * c + 1]) * p.scale),
-                    pack_bf16(__uint_as_float(kv[8 * c + 2]) * p.scale, __uint_as_float(kv[8 * c + 3]) * p.scale),
-                    pack_bf16(__uint_as_float(kv[8 * c + 4]) * p.scale, __uint_as_float(kv[8 * c + 5]) * p.scale),
-                    pack_bf16(__uint_as_float(kv[8 * c + 6]) * p.scale, __uint_as_float(kv[8 * c + 7]) * p.scale));
+                    pack_h16<F16>(__uint_as_float(kv[8 * c + 0]) * p.scale, __uint_as_float(kv[8 * c + 1]) * p.scale),
+                    pack_h16<F16>(__uint_as_float(kv[8 * c + 2]) * p.scale, __uint_as_float(kv[8 * c + 3]) * p.scale),
+                    pack_h16<F16>(__uint_as_float(kv[8 * c + 4]) * p.scale, __uint_as_float(kv[8 * c + 5]) * p.scale),
+                    pack_h16<F16>(__uint_as_float(kv[8 * c + 6]) * p.scale, __uint_as_float(kv[8 * c + 7]) * p.scale));
             fence_proxy_async_smem();
             mbar_arrive(&bar.epi_staged);
             if (issuer) {
@@ -1038,12 +1040,22 @@ __global__ void __launch_bounds__(512, 1)
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool F16>
 cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, const BwdWorkspace& ws,
                             const LaunchCommon& lc, cudaStream_t s) {
-    constexpr int kSmem = D == 64 ? Bwd64Cfg<MASK>::kSmemBytes : BwdCfg<D, MASK>::kSmemBytes;
+    constexpr int kSmem = [] {
+        if constexpr (D == 64)
+            return Bwd64Cfg<MASK>::kSmemBytes;
+        else
+            return BwdCfg<D, MASK>::kSmemBytes;
+    }();
     static_assert(kSmem <= 232448, "shared memory budget");
-    auto kernel = D == 64 ? bwd_tc64_kernel<MASK> : bwd_tc_kernel<D, MASK>;
+    auto kernel = [] {
+        if constexpr (D == 64)
+            return bwd_tc64_kernel<MASK, F16>;
+        else
+            return bwd_tc_kernel<D, MASK, F16>;
+    }();
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     const attn_fwd_params& f = prm.fwd;
@@ -1078,14 +1090,24 @@ cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, con
     return cudaGetLastError();
 }
 
+
+template <bool F16>
+cudaError_t launch_bwd_tc_dt(const attn_bwd_params& p, const BwdMaps& maps, const BwdWorkspace& ws,
+                             const LaunchCommon& lc, cudaStream_t s) {
+    const bool mask = p.fwd.mask != nullptr;
+    if (p.fwd.d == 64)
+        return mask ? launch_bwd_tc_t<64, true, F16>(p, maps, ws, lc, s)
+                    : launch_bwd_tc_t<64, false, F16>(p, maps, ws, lc, s);
+    return mask ? launch_bwd_tc_t<128, true, F16>(p, maps, ws, lc, s)
+                : launch_bwd_tc_t<128, false, F16>(p, maps, ws, lc, s);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_tc(const attn_bwd_params& p, const BwdMaps& maps, const BwdWorkspace& ws,
                           const LaunchCommon& lc, cudaStream_t s) {
-    const bool mask = p.fwd.mask != nullptr;
-    if (p.fwd.d == 64)
-        return mask ? launch_bwd_tc_t<64, true>(p, maps, ws, lc, s) : launch_bwd_tc_t<64, false>(p, maps, ws, lc, s);
-    return mask ? launch_bwd_tc_t<128, true>(p, maps, ws, lc, s) : launch_bwd_tc_t<128, false>(p, maps, ws, lc, s);
+    return p.fwd.dtype == ATTN_F16 ? launch_bwd_tc_dt<true>(p, maps, ws, lc, s)
+                                   : launch_bwd_tc_dt<false>(p, maps, ws, lc, s);
 }
 
 }  // namespace attn

@@ -94,8 +94,6 @@ struct FwdCfg {
     static constexpr int kMaskOff = kKVOff + kStages * kTileBytes;
     static constexpr int kBarOff = kMaskOff + (MASK ? 2 * kMaskBytes : 0);
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
-    static constexpr uint32_t kIdescS = idesc_bf16(BM, BN, false, false);
-    static constexpr uint32_t kIdescO = idesc_bf16(BM, D, false, true);
 };
 
 struct FwdParamsDev {
@@ -187,12 +185,15 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
         if (globaltimer() - t0 > timeout_ns) break;
 }
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool F16>
 __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_mask,
                   const FwdParamsDev p) {
     using Cfg = FwdCfg<D, MASK>;
+    // 16-bit element type of Q, K, V, P and O: bf16, or IEEE half when F16
+    constexpr uint32_t kIdescS = idesc_h16(BM, BN, false, false, F16);
+    constexpr uint32_t kIdescO = idesc_h16(BM, D, false, true, F16);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Barriers& bar = *reinterpret_cast<Barriers*>(smem + Cfg::kBarOff);
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_ss(tS, kmajor_desc(qt, kk), kmajor_desc(kt, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+                                mma_ss(tS, kmajor_desc(qt, kk), kmajor_desc(kt, kk), kIdescS, kk > 0 ? 1u : 0u);
                             mma_commit(&bar.s_full[t]);
                             if (j == nkv - 1) mma_commit(&bar.q_empty);  // last read of Q_t
                         }
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < BN / 16; ++kk)
-                                mma_ts(tO, tP + kk * 8, vmajor_desc(vt, kk), Cfg::kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
+                                mma_ts(tO, tP + kk * 8, vmajor_desc(vt, kk), kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
                             mma_commit(&bar.pv_done[t]);
                         }
                         __syncwarp();
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < BN / 16; ++kk)
-                                mma_ts(tO, tS + kk * 8, vmajor_desc(vt, kk), Cfg::kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
+                                mma_ts(tO, tS + kk * 8, vmajor_desc(vt, kk), kIdescO, (j > 1 || kk > 0) ? 1u : 0u);
                         }
                         __syncwarp();
                     }
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                         if (elect_one()) {
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                mma_ss(tS, kmajor_desc(qt, kk), kmajor_desc(kt, kk), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+                                mma_ss(tS, kmajor_desc(qt, kk), kmajor_desc(kt, kk), kIdescS, kk > 0 ? 1u : 0u);
                             mma_commit(&bar.s_full[t]);
                         }
                         __syncwarp();
@@ -523,10 +524,10 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                             for (int ch = 0; ch < 8; ++ch) {
                                 const uint4 mv = *reinterpret_cast<const uint4*>(
                                     mtile + bx * BM * 128 + r * 128 + ((ch ^ (r & 7)) << 4));
-                                const __nv_bfloat162* m2 = reinterpret_cast<const __nv_bfloat162*>(&mv);
+                                const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const float2 f = __bfloat1622float2(m2[e]);
+                                    const float2 f = unpack_h16<F16>(mw[e]);
                                     const int col = bx * 64 + ch * 8 + 2 * e;
                                     su[col] = __float_as_uint(fmaf(__uint_as_float(su[col]), p.c, f.x * kLog2e));
                                     su[col + 1] =
@@ -598,7 +599,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                             sumb = fadd2(sumb, pp);
                         else
                             suma = fadd2(suma, pp);
-                        su[i] = pack_bf16(pp.x, pp.y);
+                        su[i] = pack_h16<F16>(pp.x, pp.y);
                     }
                     if (j > 0) {  // PV of key tile j-1 has finished reading P_t and writing O_t
                         ok = mbar_wait(&bar.pv_done[t], pvcnt & 1, wc);
@@ -624,7 +625,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                                 sumb = fadd2(sumb, pp);
                             else
                                 suma = fadd2(suma, pp);
-                            pk[i] = pack_bf16(pp.x, pp.y);
+                            pk[i] = pack_h16<F16>(pp.x, pp.y);
                         }
                         tmem_st16(tS + c0 / 2, pk);
                     }
@@ -660,10 +661,10 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint4 v;
-                        v.x = pack_bf16(__uint_as_float(ov[8 * q + 0]) * inv, __uint_as_float(ov[8 * q + 1]) * inv);
-                        v.y = pack_bf16(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv);
-                        v.z = pack_bf16(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv);
-                        v.w = pack_bf16(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv);
+                        v.x = pack_h16<F16>(__uint_as_float(ov[8 * q + 0]) * inv, __uint_as_float(ov[8 * q + 1]) * inv);
+                        v.y = pack_h16<F16>(__uint_as_float(ov[8 * q + 2]) * inv, __uint_as_float(ov[8 * q + 3]) * inv);
+                        v.z = pack_h16<F16>(__uint_as_float(ov[8 * q + 4]) * inv, __uint_as_float(ov[8 * q + 5]) * inv);
+                        v.w = pack_h16<F16>(__uint_as_float(ov[8 * q + 6]) * inv, __uint_as_float(ov[8 * q + 7]) * inv);
                         dst[q] = v;
                     }
                 }
@@ -682,11 +683,11 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
     if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-template <int D, bool MASK>
+template <int D, bool MASK, bool F16>
 cudaError_t launch_tc(const attn_fwd_params& prm, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s) {
     using Cfg = FwdCfg<D, MASK>;
     static_assert(Cfg::kSmemBytes <= 232448, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<D, MASK, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     FwdParamsDev p{};
@@ -709,16 +710,22 @@ cudaError_t launch_tc(const attn_fwd_params& prm, const FwdMaps& maps, const Lau
     p.timeout_ns = lc.timeout_ns;
     p.stall_after = lc.stall_after;
     const int grid = p.num_units < lc.num_sms ? p.num_units : lc.num_sms;
-    fwd_tc_kernel<D, MASK><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(maps.q, maps.k, maps.v, maps.mask, p);
+    fwd_tc_kernel<D, MASK, F16><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(maps.q, maps.k, maps.v, maps.mask, p);
     return cudaGetLastError();
+}
+
+
+template <bool F16>
+cudaError_t launch_fwd_tc_t(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s) {
+    const bool mask = p.mask != nullptr;
+    if (p.d == 64) return mask ? launch_tc<64, true, F16>(p, maps, lc, s) : launch_tc<64, false, F16>(p, maps, lc, s);
+    return mask ? launch_tc<128, true, F16>(p, maps, lc, s) : launch_tc<128, false, F16>(p, maps, lc, s);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s) {
-    const bool mask = p.mask != nullptr;
-    if (p.d == 64) return mask ? launch_tc<64, true>(p, maps, lc, s) : launch_tc<64, false>(p, maps, lc, s);
-    return mask ? launch_tc<128, true>(p, maps, lc, s) : launch_tc<128, false>(p, maps, lc, s);
+    return p.dtype == ATTN_F16 ? launch_fwd_tc_t<true>(p, maps, lc, s) : launch_fwd_tc_t<false>(p, maps, lc, s);
 }
 
 }  // namespace attn

@@ -171,7 +171,7 @@ __device__ __forceinline__ bool aligned16(const void* p, int* err) {
 // 32-bit arithmetic when the row count allows it (IDX = unsigned), else 64-bit.
 constexpr int kRowsPerThread = 4;
 
-template <int D, typename IDX>
+template <int D, typename IDX, bool F16>
 __global__ void __launch_bounds__(256) bwd_prepass_kernel(SimtArgs a, float* stats, float* dq_acc, int* err) {
     constexpr int G = D / 8;            // threads per row
     constexpr int RPB = 256 / G;        // rows per block and step
@@ -199,12 +199,11 @@ __global__ void __launch_bounds__(256) bwd_prepass_kernel(SimtArgs a, float* sta
         if (ok) {
             const uint4 ov = *reinterpret_cast<const uint4*>(op);
             const uint4 gv = *reinterpret_cast<const uint4*>(gp);
-            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+            const uint32_t o2[4] = {ov.x, ov.y, ov.z, ov.w}, g2[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float2 of = __bfloat1622float2(o2[i]);
-                const float2 gf = __bfloat1622float2(g2[i]);
+                const float2 of = ptx::unpack_h16<F16>(o2[i]);
+                const float2 gf = ptx::unpack_h16<F16>(g2[i]);
                 sum = fmaf(of.x, gf.x, sum);
                 sum = fmaf(of.y, gf.y, sum);
             }
@@ -229,7 +228,7 @@ __global__ void __launch_bounds__(256) bwd_prepass_kernel(SimtArgs a, float* sta
 }
 
 // ------------------------------------------------------------ dQ finalize
-template <int D, typename IDX>
+template <int D, typename IDX, bool F16>
 __global__ void __launch_bounds__(256) bwd_dq_finalize_kernel(SimtArgs a, const float* dq_acc, int* err) {
     constexpr int G = D / 8;
     constexpr int RPB = 256 / G;
@@ -260,10 +259,10 @@ __global__ void __launch_bounds__(256) bwd_dq_finalize_kernel(SimtArgs a, const 
     for (int k = 0; k < kRowsPerThread; ++k) {
         if (dst[k] == nullptr) continue;
         uint4 out;
-        out.x = ptx::pack_bf16(x[k].x, x[k].y);
-        out.y = ptx::pack_bf16(x[k].z, x[k].w);
-        out.z = ptx::pack_bf16(y[k].x, y[k].y);
-        out.w = ptx::pack_bf16(y[k].z, y[k].w);
+        out.x = ptx::pack_h16<F16>(x[k].x, x[k].y);
+        out.y = ptx::pack_h16<F16>(x[k].z, x[k].w);
+        out.z = ptx::pack_h16<F16>(y[k].x, y[k].y);
+        out.w = ptx::pack_h16<F16>(y[k].z, y[k].w);
         *dst[k] = out;
     }
 }
@@ -333,39 +332,41 @@ RowGrid row_grid(long long rows, int d) {
     const long long blocks = (rows + per_block - 1) / per_block;
     return RowGrid{(unsigned)blocks, rows + blocks * rpb < (1ll << 31)};
 }
-template <int D>
+template <int D, bool F16>
 void prepass_t(const RowGrid& g, const SimtArgs& a, const BwdWorkspace& ws, int* err, cudaStream_t s) {
     if (g.idx32)
-        bwd_prepass_kernel<D, unsigned><<<g.blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
+        bwd_prepass_kernel<D, unsigned, F16><<<g.blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
     else
-        bwd_prepass_kernel<D, unsigned long long><<<g.blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
+        bwd_prepass_kernel<D, unsigned long long, F16><<<g.blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
 }
-template <int D>
+template <int D, bool F16>
 void finalize_t(const RowGrid& g, const SimtArgs& a, const BwdWorkspace& ws, int* err, cudaStream_t s) {
     if (g.idx32)
-        bwd_dq_finalize_kernel<D, unsigned><<<g.blocks, 256, 0, s>>>(a, ws.dq_acc, err);
+        bwd_dq_finalize_kernel<D, unsigned, F16><<<g.blocks, 256, 0, s>>>(a, ws.dq_acc, err);
     else
-        bwd_dq_finalize_kernel<D, unsigned long long><<<g.blocks, 256, 0, s>>>(a, ws.dq_acc, err);
+        bwd_dq_finalize_kernel<D, unsigned long long, F16><<<g.blocks, 256, 0, s>>>(a, ws.dq_acc, err);
 }
 }  // namespace
 
 cudaError_t launch_bwd_prepass(const attn_bwd_params& p, const BwdWorkspace& ws, int* err, cudaStream_t s) {
     const SimtArgs a = make_bwd_args(p, ws);
     const RowGrid g = row_grid((long long)p.fwd.B * p.fwd.H * ((p.fwd.N + 127) / 128 * 128), p.fwd.d);
+    const bool f16 = p.fwd.dtype == ATTN_F16;
     if (p.fwd.d == 64)
-        prepass_t<64>(g, a, ws, err, s);
+        f16 ? prepass_t<64, true>(g, a, ws, err, s) : prepass_t<64, false>(g, a, ws, err, s);
     else
-        prepass_t<128>(g, a, ws, err, s);
+        f16 ? prepass_t<128, true>(g, a, ws, err, s) : prepass_t<128, false>(g, a, ws, err, s);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_finalize(const attn_bwd_params& p, const BwdWorkspace& ws, int* err, cudaStream_t s) {
     const SimtArgs a = make_bwd_args(p, ws);
     const RowGrid g = row_grid((long long)p.fwd.B * p.fwd.H * p.fwd.N, p.fwd.d);
+    const bool f16 = p.fwd.dtype == ATTN_F16;
     if (p.fwd.d == 64)
-        finalize_t<64>(g, a, ws, err, s);
+        f16 ? finalize_t<64, true>(g, a, ws, err, s) : finalize_t<64, false>(g, a, ws, err, s);
     else
-        finalize_t<128>(g, a, ws, err, s);
+        f16 ? finalize_t<128, true>(g, a, ws, err, s) : finalize_t<128, false>(g, a, ws, err, s);
     return cudaGetLastError();
 }
 

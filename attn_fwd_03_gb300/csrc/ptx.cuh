@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace attn {
 namespace ptx {
@@ -302,6 +303,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same with the A/B element type chosen: fp16 (type code 0) or bf16 (1).
+__host__ __device__ constexpr uint32_t idesc_h16(int M, int N, bool a_mn, bool b_mn, bool f16) {
+    return f16 ? (idesc_bf16(M, N, a_mn, b_mn) & ~((7u << 7) | (7u << 10))) : idesc_bf16(M, N, a_mn, b_mn);
+}
 
 // Shared-memory matrix descriptor with the 128-byte swizzle:
 //   [0,14) start >> 4   [16,30) leading byte offset >> 4   [32,46) stride byte offset >> 4
@@ -352,6 +357,34 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// 16-bit storage types: F16 = false is bfloat16, true is IEEE half.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_h16(float lo, float hi) {
+    if constexpr (F16)
+        return pack_f16(lo, hi);
+    else
+        return pack_bf16(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ float2 unpack_h16(uint32_t v) {
+    if constexpr (F16) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&v));
+    } else {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+    }
+}
+template <bool F16>
+__device__ __forceinline__ float h16_to_float(uint16_t v) {
+    if constexpr (F16)
+        return __half2float(__ushort_as_half(v));
+    else
+        return __bfloat162float(__ushort_as_bfloat16(v));
 }
 
 }  // namespace ptx

@@ -436,10 +436,10 @@ def run_ours(args, w, rank, world, local_rank):
     if world == 1 and not args.no_all:
         peak = peaks["bf16_tflops"]
         table = {}
-        for idx, wk in W.WORKLOADS.items():
+        for idx, wk in {**W.WORKLOADS, **W.F16_WORKLOADS}.items():
             r = measure_workload(A, wk, 10, 3, dev, flush)
             for key in ("fwd", "bwd"):
-                if f"{key}_tflops" in r and wk.dtype == "bf16":
+                if f"{key}_tflops" in r and wk.dtype in ("bf16", "f16"):
                     r[f"{key}_pct_of_peak"] = 100.0 * r[f"{key}_tflops"] / peak
             table[wk.name] = r
         line["workloads"] = table

@@ -63,7 +63,9 @@ typedef enum attn_status_t {
 
 typedef enum attn_dtype_t {
     ATTN_BF16 = 0, /* bfloat16 storage, fp32 accumulation (tcgen05 tensor cores) */
-    ATTN_F32 = 1   /* float32 storage and arithmetic (CUDA cores; forward only)   */
+    ATTN_F32 = 1,  /* float32 storage and arithmetic (CUDA cores; forward only)   */
+    ATTN_F16 = 2   /* IEEE half storage, fp32 accumulation (tcgen05 tensor cores);
+                      P, dS and O are rounded to half as bf16 rounds them for bf16 */
 } attn_dtype_t;
 
 /*
@@ -95,7 +97,8 @@ typedef struct attn_fwd_params {
 /*
  * Backward problem: dQ, dK, dV of sum(dO * O) for the forward described by
  * `fwd`, whose o and lse (as written by attn_fwd) are READ here. Recomputes
- * S and P tile by tile; no gradient flows to the mask. bf16 only.
+ * S and P tile by tile; no gradient flows to the mask. bf16 and fp16
+ * (ATTN_F32 returns ATTN_ERR_UNSUPPORTED).
  */
 typedef struct attn_bwd_params {
     attn_fwd_params fwd;
@@ -111,7 +114,7 @@ typedef struct attn_bwd_params {
     size_t workspace_bytes;
 } attn_bwd_params;
 
-/* Forward pass (both dtypes). */
+/* Forward pass (every dtype). */
 ATTN_API attn_status_t attn_fwd(const attn_fwd_params *p, void *stream);
 
 /* Bytes of workspace attn_bwd needs for this problem (0 for an empty one):

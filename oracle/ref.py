@@ -44,9 +44,10 @@ fp64 exactly); everything is computed in fp64.
 
 Stored output. The backward consumes the O that the forward stored, and the
 library stores O in the dtype of Q. `attention_backward(..., o_storage=
-"bf16")` therefore also models that storage: the oracle rounds its own fp64 O
-to fp32 and then to bf16 (round to nearest even, as the kernels do from their
-fp32 accumulators) and takes D = rowsum(dO * O_stored) from it. Nothing else
+"bf16")` (or "f16") therefore also models that storage: the oracle rounds its
+own fp64 O to fp32 and then to bf16 or half (round to nearest even, as the
+kernels do from their fp32 accumulators) and takes D = rowsum(dO * O_stored)
+from it. Nothing else
 changes; with o_storage=None the result is the pure mathematical gradient.
 
 Parity pins: every function here is pinned by tests/test_oracle.py against
@@ -76,6 +77,16 @@ def round_bf16(x) -> np.ndarray:
     finite = np.isfinite(f)
     out = np.where(finite, r, u & 0xFFFF0000).astype(np.uint32)
     return out.view(np.float32).astype(np.float64)
+
+
+def round_f16(x) -> np.ndarray:
+    """fp64 -> fp32 -> IEEE half (round to nearest, ties to even; beyond the
+    largest finite half, 65504, the result is infinite), returned as fp64."""
+    with np.errstate(over="ignore"):
+        return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float64)
+
+
+_STORAGE = {"bf16": round_bf16, "f16": round_f16}
 
 
 def _mask_for_head(mask: Optional[np.ndarray], b: int, h: int) -> Optional[np.ndarray]:
@@ -154,8 +165,9 @@ def backward_head(qh, kh, vh, doh, scale: float, causal: bool = False, maskh=Non
     """Gradients of one head, by the closed form in the module docstring.
 
     Returns (dq[q_rows], dk[k_rows], dv[k_rows], D, D_from_o) where D and
-    D_from_o cover every query row. With o_storage="bf16", D is taken from
-    the bf16-rounded O (the stored output) instead of from P and dP.
+    D_from_o cover every query row. With o_storage="bf16" (or "f16"), D is
+    taken from the bf16- (or half-) rounded O (the stored output) instead of
+    from P and dP.
     dK and dV of a key need every query row, so the whole head is always
     swept; `q_rows` / `k_rows` only select which gradient rows are returned
     (None = all).
@@ -178,8 +190,8 @@ def backward_head(qh, kh, vh, doh, scale: float, causal: bool = False, maskh=Non
         o_rows = p @ vh
         dp = doh[r] @ vh.T
         D_o[r] = (doh[r] * o_rows).sum(axis=1)
-        if o_storage == "bf16":
-            d_rows = (doh[r] * round_bf16(o_rows)).sum(axis=1)
+        if o_storage in _STORAGE:
+            d_rows = (doh[r] * _STORAGE[o_storage](o_rows)).sum(axis=1)
         elif o_storage is None:
             d_rows = (p * dp).sum(axis=1)
         else:

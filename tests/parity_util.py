@@ -18,6 +18,11 @@ Tolerances (written here once, used by every parity test):
     itself sees when it takes D from its own bf16-rounded O instead of the
     exact one. Both come from the oracle alone; for non-degenerate shapes
     delta is ~1e-3.
+  * IEEE half inputs (an extension; no tolerance is stated for them). Half
+    keeps 10 fraction bits against bf16's 7, so every rounding in the path
+    (inputs, P, dS, O, dQ/dK/dV) is 8x finer; the bf16 bounds are scaled by
+    1/8 and rounded up: max-abs <= 4e-3 and rel-L2 <= 1e-3 (gradients: the
+    same derived allowance, with delta taken from a half-rounded O).
 """
 from __future__ import annotations
 
@@ -26,6 +31,8 @@ import torch
 
 BF16_ATOL = 2e-2
 BF16_REL_L2 = 5e-3
+F16_ATOL = 4e-3
+F16_REL_L2 = 1e-3
 F32_ATOL = 1e-4
 LSE_ATOL = 1e-3
 
@@ -45,12 +52,18 @@ def errors(got, want):
     return max_abs, rel
 
 
+def _bounds(dtype):
+    return (F16_ATOL, F16_REL_L2) if dtype == torch.float16 else (BF16_ATOL, BF16_REL_L2)
+
+
 def assert_close_bf16(name, got, want, relative_max=False):
+    """16-bit outputs: the bf16 bounds, or the half bounds when `got` is half."""
+    atol, rtol = _bounds(got.dtype if isinstance(got, torch.Tensor) else None)
     g, w = to64(got), to64(want)
     max_abs, rel = errors(g, w)
-    bound = BF16_ATOL * (max(1.0, float(np.max(np.abs(w)))) if (relative_max and w.size) else 1.0)
-    assert max_abs <= bound and rel <= BF16_REL_L2, \
-        f"{name}: max-abs {max_abs:.3e} (bound {bound:.3e}), rel-L2 {rel:.3e} (bound {BF16_REL_L2:.1e})"
+    bound = atol * (max(1.0, float(np.max(np.abs(w)))) if (relative_max and w.size) else 1.0)
+    assert max_abs <= bound and rel <= rtol, \
+        f"{name}: max-abs {max_abs:.3e} (bound {bound:.3e}), rel-L2 {rel:.3e} (bound {rtol:.1e})"
     return max_abs, rel
 
 
@@ -81,11 +94,12 @@ def assert_masked_rows_zero(o, lse_ref):
 
 def assert_grad(name, got, pure, stored):
     """Gradient check with the stored-output allowance described above."""
+    atol, rtol = _bounds(got.dtype if isinstance(got, torch.Tensor) else None)
     g, w, st = to64(got), to64(pure), to64(stored)
     delta_abs, delta = errors(st, w)
     max_abs, rel = errors(g, w)
-    bound_abs = BF16_ATOL * max(1.0, float(np.max(np.abs(w))) if w.size else 1.0) + 2 * delta_abs
-    bound_rel = BF16_REL_L2 + 2 * delta
+    bound_abs = atol * max(1.0, float(np.max(np.abs(w))) if w.size else 1.0) + 2 * delta_abs
+    bound_rel = rtol + 2 * delta
     assert max_abs <= bound_abs and rel <= bound_rel, \
         f"{name}: max-abs {max_abs:.3e} (bound {bound_abs:.3e}), rel-L2 {rel:.3e} (bound {bound_rel:.3e})"
     return max_abs, rel

@@ -71,7 +71,7 @@ def _check_fwd(o, lse, inp, causal, scale, f32=False):
 def _check_bwd(grads, inp, causal, scale):
     args = (to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), to64(inp["do"]), scale, causal,
             _oracle_mask(inp.get("mask")))
-    stored = ref.attention_backward(*args, o_storage="bf16")
+    stored = ref.attention_backward(*args, o_storage="f16" if inp["q"].dtype == torch.float16 else "bf16")
     pure = ref.attention_backward(*args)
     for i, (name, g) in enumerate(zip(("dQ", "dK", "dV"), grads)):
         assert_grad(name, g, pure[i], stored[i])
@@ -239,3 +239,63 @@ def test_full_size_backward_sampled(A, idx):
         assert_grad(name, g[b, h, rows], pure[i], stored[i])
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()
+
+
+# ------------------------------------------------------------- IEEE half
+@pytest.mark.parametrize("idx,shape", [
+    (2, (2, 3, 300, 64)),
+    (3, (1, 2, 1000, 128)),
+    (4, (2, 2, 520, 128)),
+    (5, (1, 2, 777, 128)),
+])
+def test_fp16_reduced_workloads(A, idx, shape):
+    w = W.with_dtype(W.WORKLOADS[idx], "f16")
+    inp = W.make_inputs(w, with_grad=True, shape=shape)
+    o, lse = _run_fwd(A, inp, w.causal, w.scale)
+    assert o.dtype == torch.float16
+    _check_fwd(o, lse, inp, w.causal, w.scale)
+    _check_bwd(_run_bwd(A, inp, w.causal, w.scale, o, lse), inp, w.causal, w.scale)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 129, 257])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp16_edge_lengths(A, d, N, causal):
+    inp = {n: W.random_tensor((1, 2, N, d), 150 + i, torch.float16) for i, n in enumerate(("q", "k", "v", "do"))}
+    scale = 1 / math.sqrt(d)
+    o, lse = _run_fwd(A, inp, causal, scale)
+    _check_fwd(o, lse, inp, causal, scale)
+    _check_bwd(_run_bwd(A, inp, causal, scale, o, lse), inp, causal, scale)
+
+
+def test_fp16_additive_mask(A):
+    B, H, N, d = 2, 2, 300, 64
+    inp = {n: W.random_tensor((B, H, N, d), 450 + i, torch.float16) for i, n in enumerate(("q", "k", "v", "do"))}
+    g = torch.Generator().manual_seed(8)
+    mask = torch.randn(B, 1, N, N, generator=g) * 2
+    mask[torch.rand(mask.shape, generator=g) < 0.2] = float("-inf")
+    mask[:, :, 33, :] = float("-inf")
+    inp["mask"] = mask.to(torch.float16)
+    for causal in (False, True):
+        o, lse = _run_fwd(A, inp, causal, 0.125)
+        _check_fwd(o, lse, inp, causal, 0.125)
+        _check_bwd(_run_bwd(A, inp, causal, 0.125, o, lse), inp, causal, 0.125)
+
+
+def test_fp16_benchmark_shape_sampled(A):
+    w = W.F16_WORKLOADS[6]
+    inp = W.make_inputs(w)
+    o, lse = _run_fwd(A, inp, w.causal, w.scale)
+    dq, dk, dv = _run_bwd(A, inp, w.causal, w.scale, o, lse)
+    b, h = w.B - 1, w.H // 2
+    rows = _sample_rows(w.N, 64, 99)
+    O, L = ref.forward_head(to64(inp["q"][b, h]), to64(inp["k"][b, h]), to64(inp["v"][b, h]), w.scale, w.causal,
+                            None, rows=rows)
+    assert_close_bf16("O", o[b, h, rows], O)
+    assert_lse(lse[b, h, rows], L)
+    hargs = (to64(inp["q"][b, h]), to64(inp["k"][b, h]), to64(inp["v"][b, h]), to64(inp["do"][b, h]), w.scale,
+             w.causal, None)
+    pure = ref.backward_head(*hargs, q_rows=rows, k_rows=rows)
+    stored = ref.backward_head(*hargs, q_rows=rows, k_rows=rows, o_storage="f16")
+    for i, (name, g) in enumerate((("dQ", dq), ("dK", dk), ("dV", dv))):
+        assert_grad(name, g[b, h, rows], pure[i], stored[i])

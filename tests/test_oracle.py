@@ -529,3 +529,37 @@ def test_backward_with_stored_bf16_output():
     assert 0 < np.max(np.abs(dq2 - dq)) < 0.05 * np.max(np.abs(dq))
     with pytest.raises(ValueError):
         ref.attention_backward(q, k, v, do, 0.5, True, mask, o_storage="fp8")
+
+
+def test_round_f16_ties_overflow_and_subnormals():
+    # IEEE half: 10 fraction bits, largest finite 65504, smallest subnormal 2^-24
+    u = 2.0 ** -10  # spacing just above 1
+    cases = [
+        (1.0 + u / 2, 1.0),                    # tie between 1 and 1+u: to even (1)
+        (1.0 + 3 * u / 2, 1.0 + 2 * u),        # tie between 1+u and 1+2u: to even (1+2u)
+        (1.0 + u / 2 + 2.0 ** -20, 1.0 + u),   # just above the tie: up
+        (65504.0, 65504.0),
+        (65519.0, 65504.0),                    # below the midpoint to 65536: stays finite
+        (65520.0, np.inf),                     # the midpoint rounds to even, i.e. overflows
+        (-70000.0, -np.inf),
+        (2.0 ** -25, 0.0),                     # tie between 0 and 2^-24: to even (0)
+        (3 * 2.0 ** -25, 2.0 ** -23),          # tie between 2^-24 and 2^-23: to even (2^-23)
+        (2.0 ** -24, 2.0 ** -24),
+        (0.1, 1638.0 / 16384.0),               # 0.1 = 1.6 * 2^-4 -> 1.599609375 * 2^-4
+    ]
+    x = np.array([c[0] for c in cases])
+    want = np.array([c[1] for c in cases])
+    assert np.array_equal(ref.round_f16(x), want)
+
+
+def test_backward_with_stored_f16_output():
+    q, k, v, mask = _tiny_case(34, 1, 2, 40, 8, True, True)
+    do = _rng(35).standard_normal(q.shape)
+    dq, dk, dv, D = ref.attention_backward(q, k, v, do, 0.5, True, mask)
+    dq2, dk2, dv2, D2 = ref.attention_backward(q, k, v, do, 0.5, True, mask, o_storage="f16")
+    o, _ = ref.attention_forward(q, k, v, 0.5, True, mask)
+    assert np.allclose(D2, (do * ref.round_f16(o)).sum(-1), rtol=0, atol=1e-12)
+    assert np.array_equal(dv, dv2)
+    # half keeps 3 more fraction bits than bf16: the D perturbation is about 8x smaller
+    _, _, _, D3 = ref.attention_backward(q, k, v, do, 0.5, True, mask, o_storage="bf16")
+    assert np.max(np.abs(D2 - D)) < np.max(np.abs(D3 - D))

@@ -40,7 +40,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str  # "bf16" or "f32"
+    dtype: str  # "bf16", "f16" or "f32"
     causal: bool
     mask: bool
     backward: bool
@@ -49,7 +49,7 @@ class Workload:
 
     @property
     def torch_dtype(self) -> torch.dtype:
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        return {"bf16": torch.bfloat16, "f16": torch.float16}.get(self.dtype, torch.float32)
 
     @property
     def scale(self) -> float:
@@ -69,6 +69,10 @@ class Workload:
         }
 
 
+# The benchmark workload with IEEE half storage (an extension beyond the five
+# configurations: same shape, values and flags).
+F16_WORKLOADS: Dict[int, Workload] = {}
+
 WORKLOADS: Dict[int, Workload] = {
     1: Workload(1, "one_head_n256_d64_f32_fwd", 1, 1, 256, 64, "f32", False, False, False),
     2: Workload(2, "b4_h16_n2048_d64_bf16_causal_fwd_bwd", 4, 16, 2048, 64, "bf16", True, False, True),
@@ -77,6 +81,14 @@ WORKLOADS: Dict[int, Workload] = {
                 True, qk_mult=math.sqrt(30.0), masked_row_frac=0.01),
     5: Workload(5, "b1_h16_n32768_d128_bf16_causal_fwd_bwd", 1, 16, 32768, 128, "bf16", True, False, True),
 }
+
+
+F16_WORKLOADS[6] = dataclasses.replace(WORKLOADS[2], index=6, name="b4_h16_n2048_d64_f16_causal_fwd_bwd", dtype="f16")
+
+
+def with_dtype(w: Workload, dtype: str) -> Workload:
+    """The same workload (shape, seeds, flags) stored in another dtype."""
+    return dataclasses.replace(w, dtype=dtype)
 
 
 def _normal(shape, seed: int) -> torch.Tensor:
