@@ -35,7 +35,8 @@ STATUS_NAMES = {
 }
 
 # every symbol include/attn.h declares
-EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_size", "attn_status", "attn_last_error",
+EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_size", "attn_decode",
+            "attn_decode_workspace_size", "attn_status", "attn_last_error",
             "attn_set_wait_timeout_ns", "attn_debug_set_producer_stall", "attn_debug_set_bwd_events",
             "attn_version")
 
@@ -64,6 +65,18 @@ class BwdParams(ctypes.Structure):
     ]
 
 
+class DecodeParams(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("nq", ctypes.c_int32), ("nk", ctypes.c_int32),
+        ("d", ctypes.c_int32), ("dtype", ctypes.c_int32), ("causal", ctypes.c_int32), ("scale", ctypes.c_float),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("o", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("q_stride", _i64x3), ("k_stride", _i64x3), ("v_stride", _i64x3), ("o_stride", _i64x3),
+        ("num_splits", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
 class AttnError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
@@ -82,6 +95,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd_noalloc.restype = ctypes.c_int
     lib.attn_bwd_workspace_size.argtypes = [ctypes.POINTER(FwdParams)]
     lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.attn_decode.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_void_p]
+    lib.attn_decode.restype = ctypes.c_int
+    lib.attn_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeParams)]
+    lib.attn_decode_workspace_size.restype = ctypes.c_size_t
     lib.attn_status.argtypes = [ctypes.c_void_p]
     lib.attn_status.restype = ctypes.c_int
     lib.attn_last_error.argtypes = []
@@ -217,6 +234,45 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, *, scale: Optional[float] = None, ca
     bp.workspace, bp.workspace_bytes = None, 0
     _check(lib.attn_bwd_noalloc(ctypes.byref(bp), ctypes.c_void_p(_stream_handle(stream))))
     return dq, dk, dv
+
+
+def decode_params(q, k, v, o, lse, scale: float, causal: bool, num_splits: int = 0) -> DecodeParams:
+    B, H, nq, d = q.shape
+    p = DecodeParams()
+    p.B, p.H, p.nq, p.nk, p.d = B, H, nq, k.shape[2], d
+    p.dtype = _dtype_code(q.dtype)
+    p.causal = 1 if causal else 0
+    p.scale = float(scale)
+    p.q, p.k, p.v, p.o, p.lse = _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse)
+    p.q_stride, p.k_stride, p.v_stride, p.o_stride = _strides3(q), _strides3(k), _strides3(v), _strides3(o)
+    p.num_splits = int(num_splits)
+    return p
+
+
+def decode_workspace_size(q, k, v, *, causal: bool = False, num_splits: int = 0) -> int:
+    """Bytes of workspace attn_decode needs for these shapes."""
+    o = q  # only shapes and strides are read
+    lse = q
+    return int(lib.attn_decode_workspace_size(ctypes.byref(decode_params(q, k, v, o, lse, 1.0, causal,
+                                                                          num_splits))))
+
+
+def attn_decode(q, k, v, *, scale: Optional[float] = None, causal: bool = False, out=None, lse=None,
+                workspace=None, num_splits: int = 0, stream=None):
+    """Split-KV decode: q [B, H, nq <= 16, d] against k, v [B, H, nk, d]. With causal the
+    queries are the last nq positions. Returns (O, LSE)."""
+    B, H, nq, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty((B, H, nq, d), dtype=q.dtype, device=q.device) if out is None else out
+    lse = torch.empty((B, H, nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    p = decode_params(q, k, v, out, lse, scale, causal, num_splits)
+    if workspace is None:
+        need = int(lib.attn_decode_workspace_size(ctypes.byref(p)))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    p.workspace, p.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    _check(lib.attn_decode(ctypes.byref(p), ctypes.c_void_p(_stream_handle(stream))))
+    return out, lse
 
 
 def attn_status(stream=None) -> int:

@@ -195,6 +195,34 @@ attn_status_t build_fwd_maps(const attn_fwd_params& p, FwdMaps* m) {
     return ATTN_OK;
 }
 
+// Checks of a decode problem (all but the workspace). *empty = nothing to compute.
+attn_status_t check_decode(const attn_decode_params* p, bool* empty) {
+    if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
+    if (p->B < 0 || p->H < 0 || p->nq < 0)
+        return fail(ATTN_ERR_INVALID, "negative size B=%d H=%d nq=%d", p->B, p->H, p->nq);
+    if (p->nk < 1) return fail(ATTN_ERR_INVALID, "nk must be at least 1, got %d", p->nk);
+    if (p->dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "decode is built for bf16 and fp16 only");
+    if (p->dtype != ATTN_BF16 && p->dtype != ATTN_F16) return fail(ATTN_ERR_INVALID, "unknown dtype %d", p->dtype);
+    if (p->causal != 0 && p->causal != 1) return fail(ATTN_ERR_INVALID, "causal must be 0 or 1, got %d", p->causal);
+    if (p->reserved0 != 0) return fail(ATTN_ERR_INVALID, "reserved0 must be 0");
+    if (p->num_splits < 0) return fail(ATTN_ERR_INVALID, "num_splits must be >= 0");
+    if (!std::isfinite(p->scale) || !(p->scale > 0.f))
+        return fail(ATTN_ERR_INVALID, "scale must be positive and finite");
+    if (p->d != 64 && p->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not built (64 or 128)", p->d);
+    if (p->nq > 16) return fail(ATTN_ERR_UNSUPPORTED, "decode takes at most 16 query rows, got %d", p->nq);
+    if ((long long)p->B * p->H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B * H is limited to 65535");
+    *empty = (p->B == 0 || p->H == 0 || p->nq == 0);
+    if (*empty) return ATTN_OK;
+    attn_status_t st;
+    if ((st = check_tensor("q", p->q, p->q_stride, 2, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("k", p->k, p->k_stride, 2, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("v", p->v, p->v_stride, 2, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("o", p->o, p->o_stride, 2, false)) != ATTN_OK) return st;
+    if (!p->lse) return fail(ATTN_ERR_INVALID, "lse is NULL");
+    if (misaligned_ptr(p->lse)) return fail(ATTN_ERR_ALIGN, "lse is not 16-byte aligned");
+    return ATTN_OK;
+}
+
 attn_status_t build_bwd_maps(const attn_bwd_params& p, BwdMaps* m) {
     FwdMaps f;
     attn_status_t st = build_fwd_maps(p.fwd, &f);
@@ -335,6 +363,32 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
     if ((e = record_bwd_event(2, s)) == cudaSuccess) e = launch_bwd_dq_finalize(*p, ws, lc.err, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dQ finalize launch");
     if ((e = record_bwd_event(3, s)) != cudaSuccess) return cuda_fail(e, "attn_bwd event record");
+    return ATTN_OK;
+}
+
+size_t attn_decode_workspace_size(const attn_decode_params* p) {
+    bool empty = false;
+    if (check_decode(p, &empty) != ATTN_OK || empty) return 0;
+    LaunchCommon lc;
+    if (device_setup(&lc) != ATTN_OK) return 0;
+    return decode_split_plan(*p, lc.num_sms).workspace_bytes;
+}
+
+attn_status_t attn_decode(const attn_decode_params* p, void* stream) {
+    bool empty = false;
+    attn_status_t st = check_decode(p, &empty);
+    if (st != ATTN_OK || empty) return st;
+    LaunchCommon lc;
+    if ((st = device_setup(&lc)) != ATTN_OK) return st;
+    const DecodeSplit plan = decode_split_plan(*p, lc.num_sms);
+    if (!p->workspace) return fail(ATTN_ERR_INVALID, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)
+        return fail(ATTN_ERR_ALIGN, "workspace is not 256-byte aligned");
+    if (p->workspace_bytes < plan.workspace_bytes)
+        return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", p->workspace_bytes,
+                    plan.workspace_bytes);
+    cudaError_t e = launch_decode(*p, plan, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
     return ATTN_OK;
 }
 

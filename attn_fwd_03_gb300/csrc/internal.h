@@ -52,6 +52,16 @@ BwdWorkspace bwd_workspace_at(void* base, const attn_fwd_params& f);
 attn_status_t bwd_launch_with(const attn_bwd_params& p, const BwdWorkspace& ws, void* stream);
 attn_status_t build_dq_acc_map(const attn_fwd_params& p, float* dq_acc, CUtensorMap* m);
 
+// attn_decode.cu — split-KV decode. The plan (key ranges per (b, h) and their
+// length) fixes the workspace size, so the host API and the launch share it.
+struct DecodeSplit {
+    int splits;
+    int chunk;  // keys per range, a multiple of 64
+    size_t workspace_bytes;
+};
+DecodeSplit decode_split_plan(const attn_decode_params& p, int num_sms);
+cudaError_t launch_decode(const attn_decode_params& p, const DecodeSplit& plan, cudaStream_t s);
+
 // attn_fwd_sm103.cu — tcgen05 forward (bf16).
 cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);
 

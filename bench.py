@@ -442,6 +442,8 @@ def run_ours(args, w, rank, world, local_rank):
                 if f"{key}_tflops" in r and wk.dtype in ("bf16", "f16"):
                     r[f"{key}_pct_of_peak"] = 100.0 * r[f"{key}_tflops"] / peak
             table[wk.name] = r
+        for nq in (1, 8):
+            table[f"decode_b8_h32_nq{nq}_nk8192_d128_bf16_causal"] = measure_decode(A, dev, peaks["hbm_gbs"], nq)
         line["workloads"] = table
     if world == 1 and not args.no_cpu_baseline:
         el, fl, heads = oracle_sample(w, args.cpu_budget)
@@ -449,6 +451,36 @@ def run_ours(args, w, rank, world, local_rank):
                                 "sample": f"{heads} whole head(s) of the workload, fp64 forward+backward, "
                                           f"{el:.1f} s"}
     print(json.dumps(line), flush=True)
+
+
+def measure_decode(A, dev, hbm_gbs: float, nq: int, B: int = 8, H: int = 32, nk: int = 8192, d: int = 128,
+                   steps: int = 20, warmup: int = 3) -> dict:
+    """Split-KV decode: nq query rows against an nk-key cache per (b, h). Bound by HBM: the
+    algorithmic bytes are K and V read once plus Q, O and LSE. K and V (1 GiB here) exceed L2."""
+    import torch
+    q = W.random_tensor((B, H, nq, d), 730, torch.bfloat16).to(dev)
+    k = W.random_tensor((B, H, nk, d), 731, torch.bfloat16).to(dev)
+    v = W.random_tensor((B, H, nk, d), 732, torch.bfloat16).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, nq), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(A.decode_workspace_size(q, k, v, causal=True), 1), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        A.attn_decode(q, k, v, causal=True, out=o, lse=lse, workspace=ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        A.attn_decode(q, k, v, causal=True, out=o, lse=lse, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    if A.attn_status() != A.ATTN_OK:
+        raise RuntimeError(A.last_error())
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = 2 * B * H * nk * d * 2 + 2 * B * H * nq * d * 2 + B * H * nq * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"shape": [B, H, nq, nk, d], "dtype": "bf16", "causal": True, "ms": ms,
+            "achieved_gbs": gbs, "pct_of_hbm_peak": 100.0 * gbs / hbm_gbs, "launches": 2,
+            "bytes": nbytes}
 
 
 def captured_traffic(kernel: str, workload: str):

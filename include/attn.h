@@ -146,6 +146,47 @@ ATTN_API attn_status_t attn_bwd(const attn_bwd_params *p, void *stream);
  *    earlier calls. */
 ATTN_API attn_status_t attn_bwd_noalloc(const attn_bwd_params *p, void *stream);
 
+/*
+ * Decode problem ("FlashAttention", "What it does not do": a decode step reads
+ * the whole key/value cache for a few query rows, and what helps is splitting
+ * that read across the sequence; "Explain FlashAttention and why it is
+ * IO-aware": partial (m, l, o) states merge with the same rescaling as tiles).
+ * nq query rows attend to nk >= 1 keys: O = softmax(scale * Q K^T + causal) V
+ * per (b, h), with O and LSE as attn_fwd defines them. With causal = 1 the
+ * queries are the LAST nq positions: query i sits at position nk - nq + i and
+ * sees keys j <= nk - nq + i (a query with none, when nq > nk, gets O = 0 and
+ * LSE = -inf). Layouts, alignment and dtypes (bf16 or fp16) as in
+ * attn_fwd_params, with separate query and key row counts.
+ */
+typedef struct attn_decode_params {
+    int32_t B, H;
+    int32_t nq;              /* query rows per (b, h), 1 .. 16 */
+    int32_t nk;              /* keys per (b, h), >= 1 */
+    int32_t d;               /* 64 or 128 */
+    int32_t dtype;           /* ATTN_BF16 or ATTN_F16 */
+    int32_t causal;          /* 0 or 1 (bottom-right aligned, see above) */
+    float scale;             /* > 0 */
+    const void *q;           /* [B, H, nq, d] */
+    const void *k, *v;       /* [B, H, nk, d] */
+    void *o;                 /* [B, H, nq, d], dtype of q */
+    float *lse;              /* [B, H, nq] fp32, contiguous */
+    int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3]; /* elements, (b, h, row) */
+    int32_t num_splits;      /* key ranges per (b, h); 0 = chosen by the library */
+    int32_t reserved0;       /* must be 0 */
+    void *workspace;         /* >= attn_decode_workspace_size(p) bytes, 256-byte
+                                aligned; scratch after the call */
+    size_t workspace_bytes;
+} attn_decode_params;
+
+/* Bytes of workspace attn_decode needs (the per-split partial states), for
+ * the split count it will use (p->num_splits, or its own choice when 0). */
+ATTN_API size_t attn_decode_workspace_size(const attn_decode_params *p);
+
+/* Split-KV decode: one kernel computes each split's partial (m, l, o) over
+ * its key range, a second merges the splits into O and LSE. Errors as for
+ * attn_fwd; nq outside 1 .. 16 returns ATTN_ERR_UNSUPPORTED. */
+ATTN_API attn_status_t attn_decode(const attn_decode_params *p, void *stream);
+
 /* Synchronizes `stream`, then reports (and clears) the current device's
  * error word: ATTN_ERR_TIMEOUT if a kernel gave up on a bounded wait since
  * the last call, ATTN_ERR_CUDA for an asynchronous CUDA error, else ATTN_OK. */

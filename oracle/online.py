@@ -76,6 +76,28 @@ class RowState:
             return self.o / self.l
 
 
+def merge_states(a: RowState, b: RowState) -> RowState:
+    """The state of a row whose keys are those of `a` followed by those of `b`.
+
+    Two partial states combine with the same rescaling that absorbs a tile
+    ("Explain FlashAttention and why it is IO-aware", "Keep only the state
+    needed for the final weighted average"): against the larger maximum m,
+    each state's l and o are scaled by exp(m_own - m) and added. A state that
+    saw no finite score (m = -inf, l = 0, o = 0) is the identity. This is the
+    combine step of a split-key decode ("FlashAttention", "What it does not
+    do")."""
+    out = RowState(a.o.shape[0], dtype=a.dtype)
+    if np.isneginf(a.m) and np.isneginf(b.m):
+        return out
+    m = max(a.m, b.m)
+    wa = 0.0 if np.isneginf(a.m) else np.exp(a.m - m)
+    wb = 0.0 if np.isneginf(b.m) else np.exp(b.m - m)
+    out.m = a.dtype(m)
+    out.l = a.dtype(wa * a.l + wb * b.l)
+    out.o = (wa * a.o + wb * b.o).astype(a.dtype)
+    return out
+
+
 def _check_contract(scores: np.ndarray, values: np.ndarray, tile) -> None:
     if scores.ndim != 1 or values.ndim != 2 or scores.shape[0] != values.shape[0]:
         raise ValueError("need a 1-D score vector and one value row per score")

@@ -159,6 +159,29 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, mask=None):
     return o, lse
 
 
+def decode_forward(q, k, v, scale: float, causal: bool = False):
+    """Decode: O [B,H,nq,d] and LSE [B,H,nq] for nq query rows against nk keys,
+    fp64, by the plain definition. With causal the queries are the last nq
+    positions: query i sits at position nk - nq + i and sees the keys j with
+    j <= nk - nq + i ("FlashAttention", "What it does not do": at decode the
+    query is the newest row against the whole cache). A query that sees no
+    key gets O = 0 and LSE = -inf, the all-masked policy of the forward."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, nq, _ = q.shape
+    nk = k.shape[2]
+    o = np.zeros((B, H, nq, v.shape[3]))
+    lse = np.full((B, H, nq), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            s = scale * (q[b, h] @ k[b, h].T)
+            if causal:
+                limit = nk - nq + np.arange(nq)
+                s = np.where(np.arange(nk)[None, :] > limit[:, None], -np.inf, s)
+            p, lse[b, h] = row_softmax(s)
+            o[b, h] = p @ v[b, h]
+    return o, lse
+
+
 def backward_head(qh, kh, vh, doh, scale: float, causal: bool = False, maskh=None,
                   q_rows: Optional[Sequence[int]] = None,
                   k_rows: Optional[Sequence[int]] = None, o_storage: Optional[str] = None):

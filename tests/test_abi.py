@@ -53,9 +53,10 @@ def test_struct_layout_matches_c(binding):
 #include <stddef.h>
 #include "attn.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(attn_fwd_params), offsetof(attn_fwd_params, q),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(attn_fwd_params), offsetof(attn_fwd_params, q),
          offsetof(attn_fwd_params, mask_stride), sizeof(attn_bwd_params), offsetof(attn_bwd_params, dout),
-         offsetof(attn_bwd_params, workspace_bytes));
+         offsetof(attn_bwd_params, workspace_bytes), sizeof(attn_decode_params), offsetof(attn_decode_params, q),
+         offsetof(attn_decode_params, num_splits), offsetof(attn_decode_params, workspace_bytes));
   return 0;
 }
 '''
@@ -65,9 +66,10 @@ int main(void) {
         open(c, "w").write(src)
         subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
         got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
-    F, B = binding.FwdParams, binding.BwdParams
+    F, B, Dp = binding.FwdParams, binding.BwdParams, binding.DecodeParams
     want = [ctypes.sizeof(F), F.q.offset, F.mask_stride.offset, ctypes.sizeof(B), B.dout.offset,
-            B.workspace_bytes.offset]
+            B.workspace_bytes.offset, ctypes.sizeof(Dp), Dp.q.offset, Dp.num_splits.offset,
+            Dp.workspace_bytes.offset]
     assert got == want
 
 
@@ -157,3 +159,51 @@ def test_version_and_timeout_knobs(binding):
     binding.set_wait_timeout_ns(5)  # clamped, must not crash
     binding.set_wait_timeout_ns(2_000_000_000)
     binding.debug_set_producer_stall(0)
+
+
+def _decode_params(binding, **kw):
+    p = binding.DecodeParams()
+    p.B, p.H, p.nq, p.nk, p.d = kw.get("B", 1), kw.get("H", 2), kw.get("nq", 1), kw.get("nk", 4096), kw.get("d", 128)
+    p.dtype = kw.get("dtype", binding.ATTN_BF16)
+    p.causal = kw.get("causal", 0)
+    p.scale = kw.get("scale", 0.088)
+    p.reserved0 = kw.get("reserved0", 0)
+    p.num_splits = kw.get("num_splits", 0)
+    fake = 1 << 20  # never dereferenced: every case below fails validation first
+    for name in ("q", "k", "v", "o", "lse"):
+        setattr(p, name, kw.get(name, fake))
+    st = kw.get("stride", (4096 * 128, 4096 * 128, 128))
+    for name in ("q_stride", "k_stride", "v_stride", "o_stride"):
+        setattr(p, name, (ctypes.c_int64 * 3)(*st))
+    return p
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(nq=17), "ATTN_ERR_UNSUPPORTED"),
+    (dict(nq=-1), "ATTN_ERR_INVALID"),
+    (dict(nk=0), "ATTN_ERR_INVALID"),
+    (dict(d=96), "ATTN_ERR_UNSUPPORTED"),
+    (dict(dtype=1), "ATTN_ERR_UNSUPPORTED"),  # fp32
+    (dict(dtype=7), "ATTN_ERR_INVALID"),
+    (dict(causal=2), "ATTN_ERR_INVALID"),
+    (dict(reserved0=1), "ATTN_ERR_INVALID"),
+    (dict(num_splits=-1), "ATTN_ERR_INVALID"),
+    (dict(scale=0.0), "ATTN_ERR_INVALID"),
+    (dict(B=300, H=300), "ATTN_ERR_UNSUPPORTED"),
+    (dict(k=0), "ATTN_ERR_INVALID"),
+    (dict(lse=0), "ATTN_ERR_INVALID"),
+    (dict(v=(1 << 20) + 8), "ATTN_ERR_ALIGN"),
+    (dict(stride=(4096 * 128, 4096 * 128, 100)), "ATTN_ERR_ALIGN"),
+])
+def test_decode_argument_errors(binding, kw, status):
+    p = _decode_params(binding, **kw)
+    assert binding.lib.attn_decode(ctypes.byref(p), None) == getattr(binding, status)
+    assert binding.last_error() != ""
+    assert binding.lib.attn_decode_workspace_size(ctypes.byref(p)) == 0
+
+
+@pytest.mark.parametrize("shape", [(0, 2, 1), (2, 0, 1), (1, 1, 0)])
+def test_decode_empty_problem_is_a_no_op(binding, shape):
+    B, H, nq = shape
+    p = _decode_params(binding, B=B, H=H, nq=nq, q=0, k=0, v=0, o=0, lse=0)
+    assert binding.lib.attn_decode(ctypes.byref(p), None) == binding.ATTN_OK

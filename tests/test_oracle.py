@@ -563,3 +563,67 @@ def test_backward_with_stored_f16_output():
     # half keeps 3 more fraction bits than bf16: the D perturbation is about 8x smaller
     _, _, _, D3 = ref.attention_backward(q, k, v, do, 0.5, True, mask, o_storage="bf16")
     assert np.max(np.abs(D2 - D)) < np.max(np.abs(D3 - D))
+
+
+# ------------------------------------------------------------------ decode
+def test_decode_square_causal_is_the_causal_forward():
+    # with nq = nk the bottom-right causal alignment is the ordinary one
+    q, k, v, _ = _tiny_case(40, 2, 2, 24, 8, False, False)
+    o1, l1 = ref.decode_forward(q, k, v, 0.3, causal=True)
+    o2, l2 = ref.attention_forward(q, k, v, 0.3, causal=True)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-14) and np.allclose(l1, l2, rtol=0, atol=1e-14)
+
+
+def test_decode_rows_are_the_last_rows_of_a_causal_forward():
+    # nq query rows appended to a prefix: decode of those rows = the last rows of the causal
+    # forward over prefix + rows
+    r = _rng(41)
+    B, H, nk, nq, d = 1, 2, 37, 5, 8
+    qf = r.standard_normal((B, H, nk, d))
+    k = r.standard_normal((B, H, nk, d))
+    v = r.standard_normal((B, H, nk, d))
+    o_full, l_full = ref.attention_forward(qf, k, v, 0.4, causal=True)
+    o, l = ref.decode_forward(qf[:, :, nk - nq:], k, v, 0.4, causal=True)
+    assert np.allclose(o, o_full[:, :, nk - nq:], rtol=0, atol=1e-14)
+    assert np.allclose(l, l_full[:, :, nk - nq:], rtol=0, atol=1e-14)
+
+
+def test_decode_brute_force_and_unseen_rows():
+    r = _rng(42)
+    nq, nk, d = 6, 4, 3
+    q, k, v = r.standard_normal((1, 1, nq, d)), r.standard_normal((1, 1, nk, d)), r.standard_normal((1, 1, nk, d))
+    for causal in (False, True):
+        o, lse = ref.decode_forward(q, k, v, 0.7, causal)
+        for i in range(nq):
+            keys = [j for j in range(nk) if not causal or j <= nk - nq + i]
+            if not keys:  # nq > nk: the first rows see no key
+                assert np.all(o[0, 0, i] == 0) and np.isneginf(lse[0, 0, i])
+                continue
+            s = [0.7 * sum(q[0, 0, i, t] * k[0, 0, j, t] for t in range(d)) for j in keys]
+            mx = max(s)
+            w = [math.exp(x - mx) for x in s]
+            want = [sum(w[a] * v[0, 0, j, t] for a, j in enumerate(keys)) / sum(w) for t in range(d)]
+            assert np.allclose(o[0, 0, i], want, rtol=0, atol=1e-13)
+            assert abs(lse[0, 0, i] - (mx + math.log(sum(w)))) < 1e-13
+
+
+def test_merged_states_equal_the_whole_row():
+    r = _rng(43)
+    s = r.standard_normal(50) * 3
+    s[10:14] = -np.inf
+    vals = r.standard_normal((50, 4))
+    whole = online.RowState(4)
+    whole.absorb(s, vals)
+    for cut in (0, 1, 13, 25, 49, 50):
+        a, b = online.RowState(4), online.RowState(4)
+        if cut > 0:
+            a.absorb(s[:cut], vals[:cut])
+        if cut < 50:
+            b.absorb(s[cut:], vals[cut:])
+        m = online.merge_states(a, b)
+        assert abs(m.m - whole.m) == 0
+        assert abs(m.l - whole.l) < 1e-12 * whole.l
+        assert np.allclose(m.result(), whole.result(), rtol=0, atol=1e-14)
+    empty = online.RowState(4)
+    e = online.merge_states(empty, online.RowState(4))
+    assert np.isneginf(e.m) and e.l == 0 and np.all(e.result() == 0)
