@@ -13,10 +13,13 @@
 //
 // The work is bound by HBM bandwidth (every key and value is read once, at
 // about nq FLOP per byte), so the split kernel runs on the CUDA cores:
-// 64-key blocks of K and V are double-buffered in shared memory with
-// cp.async, 256 threads compute the nq x 64 scores, one warp per query row
+// 64-key blocks of K and V are staged in shared memory with cp.async,
+// 256 threads compute the nq x 64 scores, one warp per query row
 // updates (m, l) and the probabilities, and the threads accumulate o in
 // registers, each over its own subset of the keys, reduced once at the end.
+// Three blocks are in flight per CTA and, up to 8 query rows, two CTAs share
+// an SM, so about 190 KB of loads per SM cover the memory latency at full
+// bandwidth.
 // Scores are in the log2 domain: s = c * (q . k) with c = scale * log2(e).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -31,6 +34,7 @@ namespace attn {
 namespace {
 
 constexpr int KB = 64;        // keys per block iteration
+constexpr int kStages = 3;    // K/V blocks in flight per CTA (two CTAs per SM)
 constexpr int kThreads = 256;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -79,8 +83,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
 
     extern __shared__ __align__(16) uint8_t sm[];
     float* q_s = reinterpret_cast<float*>(sm);                     // [NQP][D], scaled by c
-    uint8_t* kv_s = sm + NQP * D * 4;                              // [2 buffers][K, V][KB][ROW]
-    float* p_s = reinterpret_cast<float*>(kv_s + 2 * 2 * KB * ROW);  // [NQP][KB] scores, then probabilities
+    uint8_t* kv_s = sm + NQP * D * 4;                              // [kStages buffers][K, V][KB][ROW]
+    float* p_s = reinterpret_cast<float*>(kv_s + kStages * 2 * KB * ROW);  // [NQP][KB] scores, then probabilities
     float* alpha_s = p_s + NQP * KB;                                // [NQP]
 
     const int split = blockIdx.x, bh = blockIdx.y;
@@ -124,15 +128,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
     const int kl = t % KL, pair = t / KL, pi = pair / CH, pc = pair % CH;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 
-    if (nblk > 0) stage(0, 0);
+    // one commit group per block (empty past the end), so "all but the newest kStages - 1
+    // groups complete" always means "block blk has landed"
+#pragma unroll
+    for (int st = 0; st < kStages - 1; ++st) {
+        if (st < nblk) stage(st, st);
+        else cp_async_commit();
+    }
     for (int blk = 0; blk < nblk; ++blk) {
-        const int buf = blk & 1;
-        if (blk + 1 < nblk) {
-            stage(blk + 1, buf ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
+        const int buf = blk % kStages;
+        if (blk + kStages - 1 < nblk) stage(blk + kStages - 1, (blk + kStages - 1) % kStages);
+        else cp_async_commit();
+        cp_async_wait<kStages - 1>();
         __syncthreads();  // block blk staged; previous block's probabilities consumed
         const uint8_t* k_s = kv_s + (buf * 2 + 0) * KB * ROW;
         const uint8_t* v_s = kv_s + (buf * 2 + 1) * KB * ROW;
@@ -237,6 +244,175 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(DecodeArgs a)
     }
 }
 
+// Up to four query rows: each warp streams its own keys straight into registers
+// (no shared memory, no block-wide barriers). A key row is split over LPK lanes
+// (16 bytes each), so one 16-byte load per lane covers KPI keys; every lane
+// group (the LPK lanes of one key slot) keeps its own running (m, l, o) for
+// the keys it sees, rescaling once per group of U keys, and the groups' states
+// are merged through shared memory at the end. Loads of the next group are
+// issued before the current one is used.
+template <int D, int NQP, bool F16>
+__global__ void __launch_bounds__(kThreads) decode_stream_kernel(DecodeArgs a) {
+    constexpr int LPK = D / 8;        // lanes per key row
+    constexpr int KPI = 32 / LPK;     // keys per warp-wide load
+    constexpr int U = 4;              // loads per lane per group
+    constexpr int G = KPI * U;        // keys per warp per group
+    constexpr int NW = kThreads / 32;
+    constexpr int SLOTS = NW * KPI;   // lane groups per CTA
+    __shared__ float st_m[NQP][SLOTS], st_l[NQP][SLOTS];
+    __shared__ __align__(16) float st_o[NQP][SLOTS][D];
+
+    const int split = blockIdx.x, bh = blockIdx.y;
+    const int b = bh / a.H, h = bh % a.H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot_in_warp = lane / LPK, cl = lane % LPK;
+    const int k_begin = split * a.chunk;
+    const int k_end = min(a.nk, k_begin + a.chunk);
+    const uint8_t* kbase = a.k + (b * a.k_sb + h * a.k_sh) * 2 + cl * 16;
+    const uint8_t* vbase = a.v + (b * a.v_sb + h * a.v_sh) * 2 + cl * 16;
+
+    float q[NQP][8];
+#pragma unroll
+    for (int i = 0; i < NQP; ++i) {
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (i < a.nq)
+            raw = *reinterpret_cast<const uint4*>(a.q + (b * a.q_sb + h * a.q_sh + (long long)i * a.q_sn) * 2 + cl * 16);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = ptx::unpack_h16<F16>(w[e]);
+            q[i][2 * e] = f.x * a.c;
+            q[i][2 * e + 1] = f.y * a.c;
+        }
+    }
+    float m[NQP], l[NQP], o[NQP][8];
+#pragma unroll
+    for (int i = 0; i < NQP; ++i) {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[i][e] = 0.f;
+    }
+
+    // this warp's groups: keys k_begin + (g * NW + warp) * G + u * KPI + slot_in_warp
+    const int ngroups = (k_end - k_begin + G - 1) / G;
+    auto key_of = [&](int g, int u) { return k_begin + (g * NW + warp) * G + u * KPI + slot_in_warp; };
+    auto load = [&](int g, uint4 (&kr)[U], uint4 (&vr)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            int key = key_of(g, u);
+            key = key < k_end ? key : k_end - 1;  // stay in bounds; masked below
+            kr[u] = __ldg(reinterpret_cast<const uint4*>(kbase + (long long)key * a.k_sn * 2));
+            vr[u] = __ldg(reinterpret_cast<const uint4*>(vbase + (long long)key * a.v_sn * 2));
+        }
+    };
+    uint4 kc[U], vc[U], kn[U], vn[U];
+    int g = 0;
+    if (warp < ngroups) load(0, kc, vc);
+    for (; g * NW + warp < ngroups; ++g) {
+        const bool more = (g + 1) * NW + warp < ngroups;
+        if (more) load(g + 1, kn, vn);
+        float s[NQP][U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t w[4] = {kc[u].x, kc[u].y, kc[u].z, kc[u].w};
+            float2 kf[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) kf[e] = ptx::unpack_h16<F16>(w[e]);
+            const int key = key_of(g, u);
+#pragma unroll
+            for (int i = 0; i < NQP; ++i) {
+                float x = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x = fmaf(q[i][2 * e], kf[e].x, x);
+                    x = fmaf(q[i][2 * e + 1], kf[e].y, x);
+                }
+#pragma unroll
+                for (int sh = LPK / 2; sh > 0; sh >>= 1) x += __shfl_xor_sync(kFull, x, sh);
+                const bool ok = key < k_end && i < a.nq && (!a.causal || key <= a.nk - a.nq + i);
+                s[i][u] = ok ? x : -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NQP; ++i) {
+            float mx = s[i][0];
+#pragma unroll
+            for (int u = 1; u < U; ++u) mx = fmaxf(mx, s[i][u]);
+            const float m_new = fmaxf(m[i], mx);
+            if (m_new == -INFINITY) continue;  // nothing seen yet by this lane group
+            const float alpha = ptx::ex2(m[i] - m_new);  // 0 when the group had no key yet
+            float p[U];
+            float ps = 0.f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                p[u] = ptx::ex2(s[i][u] - m_new);
+                ps += p[u];
+            }
+            l[i] = l[i] * alpha + ps;
+            m[i] = m_new;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[i][e] *= alpha;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t w[4] = {vc[u].x, vc[u].y, vc[u].z, vc[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 vf = ptx::unpack_h16<F16>(w[e]);
+                    o[i][2 * e] = fmaf(p[u], vf.x, o[i][2 * e]);
+                    o[i][2 * e + 1] = fmaf(p[u], vf.y, o[i][2 * e + 1]);
+                }
+            }
+        }
+        if (more) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                kc[u] = kn[u];
+                vc[u] = vn[u];
+            }
+        }
+    }
+
+    // merge the CTA's lane-group states into the split's partial record
+    const int slot = warp * KPI + slot_in_warp;
+#pragma unroll
+    for (int i = 0; i < NQP; ++i) {
+        if (cl == 0) {
+            st_m[i][slot] = m[i];
+            st_l[i][slot] = l[i];
+        }
+        *reinterpret_cast<float4*>(&st_o[i][slot][cl * 8]) = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+        *reinterpret_cast<float4*>(&st_o[i][slot][cl * 8 + 4]) = make_float4(o[i][4], o[i][5], o[i][6], o[i][7]);
+    }
+    __syncthreads();
+    float* rec0 = a.part + ((long long)bh * a.splits + split) * a.nq * rec_floats<D>();
+    for (int idx = threadIdx.x; idx < NQP * D; idx += kThreads) {
+        const int i = idx / D, e = idx % D;
+        if (i >= a.nq) continue;
+        float M = -INFINITY;
+        for (int sl = 0; sl < SLOTS; ++sl) M = fmaxf(M, st_m[i][sl]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+            for (int sl = 0; sl < SLOTS; ++sl) {
+                const float w = ptx::ex2(st_m[i][sl] - M);  // 0 for a group that saw no key
+                L = fmaf(w, st_l[i][sl], L);
+                O = fmaf(w, st_o[i][sl][e], O);
+            }
+        }
+        rec0[i * rec_floats<D>() + 4 + e] = O;
+        if (e == 0) {
+            rec0[i * rec_floats<D>() + 0] = M;
+            rec0[i * rec_floats<D>() + 1] = L;
+        }
+    }
+}
+
+template <int D, int NQP, bool F16>
+cudaError_t launch_stream(const DecodeArgs& a, cudaStream_t s) {
+    decode_stream_kernel<D, NQP, F16><<<dim3(a.splits, a.B * a.H), kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 // One warp per (b, h, row): merge the row's split states into O and LSE.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeArgs a) {
@@ -278,7 +454,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(DecodeArgs a) {
 template <int D, int NQP, bool F16>
 cudaError_t launch_split(const DecodeArgs& a, cudaStream_t s) {
     constexpr int ROW = D * 2 + 16;
-    constexpr size_t smem = NQP * D * 4 + 2 * 2 * KB * ROW + NQP * KB * 4 + NQP * 4;
+    constexpr size_t smem = NQP * D * 4 + kStages * 2 * KB * ROW + NQP * KB * 4 + NQP * 4;
     cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, NQP, F16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -290,11 +466,11 @@ template <int D, bool F16>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
     cudaError_t e;
     if (a.nq <= 1)
-        e = launch_split<D, 1, F16>(a, s);
+        e = launch_stream<D, 1, F16>(a, s);
     else if (a.nq <= 2)
-        e = launch_split<D, 2, F16>(a, s);
+        e = launch_stream<D, 2, F16>(a, s);
     else if (a.nq <= 4)
-        e = launch_split<D, 4, F16>(a, s);
+        e = launch_stream<D, 4, F16>(a, s);
     else if (a.nq <= 8)
         e = launch_split<D, 8, F16>(a, s);
     else
@@ -311,9 +487,10 @@ DecodeSplit decode_split_plan(const attn_decode_params& p, int num_sms) {
     const int max_splits = (p.nk + KB - 1) / KB;
     int splits = p.num_splits;
     if (splits <= 0) {
-        // about two CTAs per SM in total, each range at least 256 keys
+        // at least four waves of two CTAs per SM, so the last wave's shortfall stays small;
+        // each range at least 256 keys
         const long long bh = (long long)p.B * p.H;
-        const long long want = (2LL * num_sms + bh - 1) / (bh > 0 ? bh : 1);
+        const long long want = (8LL * num_sms + bh - 1) / (bh > 0 ? bh : 1);
         const int by_len = (p.nk + 255) / 256;
         splits = (int)(want < by_len ? want : by_len);
     }
