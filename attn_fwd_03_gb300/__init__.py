@@ -12,7 +12,7 @@ include/attn.h at the repository root.
 from ._binding import (  # noqa: F401
     ATTN_BF16, ATTN_ERR_ALIGN, ATTN_ERR_CUDA, ATTN_ERR_INVALID, ATTN_ERR_TIMEOUT, ATTN_ERR_UNSUPPORTED,
     ATTN_ERR_WORKSPACE, ATTN_F16, ATTN_F32, ATTN_OK, EXPORTED, LIB_PATH, AttnError, BwdParams, DecodeParams,
-    FwdParams, attn_bwd, attn_bwd_noalloc, attn_decode, attn_fwd, attn_status, bwd_workspace_size,
+    FwdParams, attn_bwd, attn_bwd_deterministic, attn_bwd_noalloc, attn_decode, attn_fwd, attn_status, bwd_workspace_size,
     debug_set_bwd_events, debug_set_producer_stall, decode_workspace_size, last_error, lib, set_wait_timeout_ns,
     version,
 )

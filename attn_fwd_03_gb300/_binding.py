@@ -35,7 +35,8 @@ STATUS_NAMES = {
 }
 
 # every symbol include/attn.h declares
-EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_workspace_size", "attn_decode",
+EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_deterministic", "attn_bwd_workspace_size",
+            "attn_decode",
             "attn_decode_workspace_size", "attn_status", "attn_last_error",
             "attn_set_wait_timeout_ns", "attn_debug_set_producer_stall", "attn_debug_set_bwd_events",
             "attn_version")
@@ -93,6 +94,8 @@ def _load() -> ctypes.CDLL:
     lib.attn_bwd.restype = ctypes.c_int
     lib.attn_bwd_noalloc.argtypes = [ctypes.POINTER(BwdParams), ctypes.c_void_p]
     lib.attn_bwd_noalloc.restype = ctypes.c_int
+    lib.attn_bwd_deterministic.argtypes = [ctypes.POINTER(BwdParams), ctypes.c_void_p]
+    lib.attn_bwd_deterministic.restype = ctypes.c_int
     lib.attn_bwd_workspace_size.argtypes = [ctypes.POINTER(FwdParams)]
     lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
     lib.attn_decode.argtypes = [ctypes.POINTER(DecodeParams), ctypes.c_void_p]
@@ -192,27 +195,44 @@ def bwd_workspace_size(q: torch.Tensor) -> int:
     return int(lib.attn_bwd_workspace_size(ctypes.byref(p)))
 
 
-def attn_bwd(q, k, v, o, lse, dout, *, scale: Optional[float] = None, causal: bool = False,
-             mask: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """dQ, dK, dV of sum(dout * O) by recomputation from O and LSE."""
+def _bwd_call(entry, q, k, v, o, lse, dout, scale, causal, mask, dq, dk, dv, workspace, stream):
+    """Fill attn_bwd_params and call `entry` (one of the C backward entry points).
+    workspace: a device tensor, None to allocate one here, or False for none (attn_bwd_noalloc)."""
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
     dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
     dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
-    need = bwd_workspace_size(q)
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     bp = BwdParams()
     bp.fwd = fwd_params(q, k, v, o, lse, scale, causal, mask)
     bp.dout, bp.do_stride = _ptr(dout), _strides3(dout)
     bp.dq, bp.dk, bp.dv = _ptr(dq), _ptr(dk), _ptr(dv)
     bp.dq_stride, bp.dk_stride, bp.dv_stride = _strides3(dq), _strides3(dk), _strides3(dv)
-    bp.workspace = workspace.data_ptr()
-    bp.workspace_bytes = workspace.numel() * workspace.element_size()
-    _check(lib.attn_bwd(ctypes.byref(bp), ctypes.c_void_p(_stream_handle(stream))))
+    if workspace is False:
+        bp.workspace, bp.workspace_bytes = None, 0
+    else:
+        if workspace is None:
+            workspace = torch.empty(max(bwd_workspace_size(q), 1), dtype=torch.uint8, device=q.device)
+        bp.workspace = workspace.data_ptr()
+        bp.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(entry(ctypes.byref(bp), ctypes.c_void_p(_stream_handle(stream))))
     return dq, dk, dv
+
+
+def attn_bwd(q, k, v, o, lse, dout, *, scale: Optional[float] = None, causal: bool = False,
+             mask: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of sum(dout * O) by recomputation from O and LSE."""
+    return _bwd_call(lib.attn_bwd, q, k, v, o, lse, dout, scale, causal, mask, dq, dk, dv, workspace, stream)
+
+
+def attn_bwd_deterministic(q, k, v, o, lse, dout, *, scale: Optional[float] = None, causal: bool = False,
+                           mask: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None, workspace=None,
+                           stream=None):
+    """attn_bwd with dQ summed over key tiles in a fixed order, so all three
+    gradients are the same bits on every call."""
+    return _bwd_call(lib.attn_bwd_deterministic, q, k, v, o, lse, dout, scale, causal, mask, dq, dk, dv, workspace,
+                     stream)
 
 
 def attn_bwd_noalloc(q, k, v, o, lse, dout, *, scale: Optional[float] = None, causal: bool = False,
@@ -220,20 +240,7 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, *, scale: Optional[float] = None, ca
     """attn_bwd using the library's built-in 40 MiB scratch instead of a
     workspace, for callers that must not allocate device memory at this point.
     Only the gradient outputs are allocated here (when not given)."""
-    B, H, N, d = q.shape
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
-    dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
-    dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
-    dv = torch.empty_like(v, memory_format=torch.contiguous_format) if dv is None else dv
-    bp = BwdParams()
-    bp.fwd = fwd_params(q, k, v, o, lse, scale, causal, mask)
-    bp.dout, bp.do_stride = _ptr(dout), _strides3(dout)
-    bp.dq, bp.dk, bp.dv = _ptr(dq), _ptr(dk), _ptr(dv)
-    bp.dq_stride, bp.dk_stride, bp.dv_stride = _strides3(dq), _strides3(dk), _strides3(dv)
-    bp.workspace, bp.workspace_bytes = None, 0
-    _check(lib.attn_bwd_noalloc(ctypes.byref(bp), ctypes.c_void_p(_stream_handle(stream))))
-    return dq, dk, dv
+    return _bwd_call(lib.attn_bwd_noalloc, q, k, v, o, lse, dout, scale, causal, mask, dq, dk, dv, False, stream)
 
 
 def decode_params(q, k, v, o, lse, scale: float, causal: bool, num_splits: int = 0) -> DecodeParams:

@@ -366,6 +366,34 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
     return ATTN_OK;
 }
 
+attn_status_t attn_bwd_deterministic(const attn_bwd_params* p, void* stream) {
+    bool empty = false;
+    attn_status_t st = bwd_check_inputs(p, &empty);
+    if (st != ATTN_OK || empty) return st;
+    const size_t need = bwd_workspace_bytes(p->fwd);
+    if (!p->workspace || p->workspace_bytes < need)
+        return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", p->workspace_bytes, need);
+    if ((reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)
+        return fail(ATTN_ERR_ALIGN, "workspace is not 256-byte aligned");
+    LaunchCommon lc;
+    if ((st = device_setup(&lc)) != ATTN_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const BwdWorkspace ws = bwd_workspace_split(*p);
+    BwdMaps maps;
+    if ((st = build_bwd_maps(*p, &maps)) != ATTN_OK) return st;
+    if ((st = encode_dq_acc_map(p->fwd, ws.dq_acc, &maps.dq_acc)) != ATTN_OK) return st;
+    // dK and dV come from the key-stationary kernel, whose sums over query tiles run in a
+    // fixed order; its dQ accumulator output is not used. dQ comes from the query-stationary
+    // kernel, which sums over key tiles in a fixed order and writes dQ itself.
+    cudaError_t e = launch_bwd_prepass(*p, ws, lc.err, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd_deterministic pre-pass launch");
+    if ((e = launch_bwd_tc(*p, maps, ws, lc, s)) != cudaSuccess)
+        return cuda_fail(e, "attn_bwd_deterministic dK/dV launch");
+    if ((e = launch_bwd_dq(*p, maps, ws, lc, s)) != cudaSuccess)
+        return cuda_fail(e, "attn_bwd_deterministic dQ launch");
+    return ATTN_OK;
+}
+
 size_t attn_decode_workspace_size(const attn_decode_params* p) {
     bool empty = false;
     if (check_decode(p, &empty) != ATTN_OK || empty) return 0;

@@ -15,19 +15,21 @@
 //                                      shared memory (swizzled, query-contiguous)
 //   dV += P^T dO, dK += dS^T Q         (tcgen05, A operand in tensor memory)
 //   dQ_tile = dS K                     (tcgen05, A = dS read query-major)
-// and a second warpgroup adds scale * dQ_tile into the fp32 dQ accumulator in
-// global memory with vector reductions (other key tiles add to the same rows).
+// and the warpgroups stage scale * dQ_tile in shared memory, from where a TMA
+// reduce-add puts it into the fp32 dQ accumulator in global memory (other key
+// tiles add to the same rows).
 //
 // Warp roles (12 warps):
 //   warps 0-7   two warpgroups; warpgroup g builds P^T / dS^T for query
 //               columns [64 g, 64 g + 64) of each tile (thread = key row),
-//               then drains its half of the dQ tile's columns (thread = query
+//               then stages its half of the dQ tile's columns (thread = query
 //               row); at the end warpgroup 0 writes dV and warpgroup 1 dK
 //   warp  8     TMA producer: K and V once, then per query tile Q_i, dO_i, the
 //               mask tile and the tile's -LSE*log2(e) and -D statistics (1 KB,
 //               written tile-padded by the pre-pass)
 //   warp  9     TMEM allocator and MMA issuer
-//   warps 10-11 idle
+//   warp 10     issues the TMA reduce-add of each staged dQ tile
+//   warp 11     idle
 //
 // Tensor memory (512 columns, lane = key row for S^T/dP^T/dK/dV, query row for dQ):
 //   [0,128)    S^T fp32; P^T bf16 pairs in [0,32) and [64,96) (see packed_col);

@@ -69,6 +69,11 @@ cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const L
 cudaError_t launch_bwd_tc(const attn_bwd_params& p, const BwdMaps& maps, const BwdWorkspace& ws,
                           const LaunchCommon& lc, cudaStream_t s);
 
+// attn_bwd_dq.cu — query-stationary tcgen05 dQ kernel (fixed order of additions); writes dQ
+// in the dtype of Q from the row statistics in ws.stats.
+cudaError_t launch_bwd_dq(const attn_bwd_params& p, const BwdMaps& maps, const BwdWorkspace& ws,
+                          const LaunchCommon& lc, cudaStream_t s);
+
 // attn_simt.cu — CUDA-core kernels.
 cudaError_t launch_fwd_simt(const attn_fwd_params& p, cudaStream_t s);  // fp32 inputs
 cudaError_t launch_bwd_prepass(const attn_bwd_params& p, const BwdWorkspace& ws, int* err, cudaStream_t s);

@@ -218,6 +218,9 @@ def measure_workload(A, w, steps, warmup, dev, flush):
         bwd = lambda: A.attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask,  # noqa: E731
                                  dq=dq, dk=dk, dv=dv, workspace=ws)
         calls.append(("bwd", bwd))
+        det = lambda: A.attn_bwd_deterministic(q, k, v, o, lse, do, scale=w.scale, causal=w.causal,  # noqa: E731
+                                               mask=mask, dq=dq, dk=dk, dv=dv, workspace=ws)
+        calls.append(("bwd_deterministic", det))
     for name, fn in calls:
         for _ in range(warmup):
             fwd()
@@ -236,9 +239,10 @@ def measure_workload(A, w, steps, warmup, dev, flush):
     f = W.attention_flops(w.B, w.H, w.N, w.d, w.causal)
     out["fwd_ms"] = res["fwd"]
     out["fwd_tflops"] = f / (res["fwd"] * 1e-3) / 1e12
-    if "bwd" in res:
-        out["bwd_ms"] = res["bwd"]
-        out["bwd_tflops"] = 2.5 * f / (res["bwd"] * 1e-3) / 1e12
+    for key in ("bwd", "bwd_deterministic"):  # both counted as 2.5x the forward's FLOPs
+        if key in res:
+            out[f"{key}_ms"] = res[key]
+            out[f"{key}_tflops"] = 2.5 * f / (res[key] * 1e-3) / 1e12
     return out
 
 def run_ours(args, w, rank, world, local_rank):
@@ -438,7 +442,7 @@ def run_ours(args, w, rank, world, local_rank):
         table = {}
         for idx, wk in {**W.WORKLOADS, **W.F16_WORKLOADS}.items():
             r = measure_workload(A, wk, 10, 3, dev, flush)
-            for key in ("fwd", "bwd"):
+            for key in ("fwd", "bwd", "bwd_deterministic"):
                 if f"{key}_tflops" in r and wk.dtype in ("bf16", "f16"):
                     r[f"{key}_pct_of_peak"] = 100.0 * r[f"{key}_tflops"] / peak
             table[wk.name] = r

@@ -146,6 +146,20 @@ ATTN_API attn_status_t attn_bwd(const attn_bwd_params *p, void *stream);
  *    earlier calls. */
 ATTN_API attn_status_t attn_bwd_noalloc(const attn_bwd_params *p, void *stream);
 
+/* The backward pass with every gradient reproducible bit for bit: the same
+ * inputs give the same dQ, dK and dV on every call and every run on a given
+ * GPU model. attn_bwd adds each key tile's share of a dQ row into an fp32
+ * accumulator as the tiles finish, so its dQ can differ in the last bits
+ * between runs. Here dQ comes from a second tensor-core kernel that keeps a
+ * query tile on chip, recomputes the scores and dP against every key tile
+ * in order ("What is FlashAttention?", Step 3 loop order, Step 4 recompute)
+ * and writes dQ once; dK and dV come from attn_bwd's key-stationary kernel,
+ * whose sums over query tiles already run in a fixed order.
+ *  - Arguments, workspace and errors exactly as attn_bwd.
+ *  - It does about 1.4 times the tensor-core work of attn_bwd (the scores
+ *    and dP are computed twice). Results agree with attn_bwd's to rounding. */
+ATTN_API attn_status_t attn_bwd_deterministic(const attn_bwd_params *p, void *stream);
+
 /*
  * Decode problem ("FlashAttention", "What it does not do": a decode step reads
  * the whole key/value cache for a few query rows, and what helps is splitting

@@ -117,6 +117,7 @@ def test_fwd_argument_errors(binding, kw, status):
 def test_null_params(binding):
     assert binding.lib.attn_fwd(None, None) == binding.ATTN_ERR_INVALID
     assert binding.lib.attn_bwd(None, None) == binding.ATTN_ERR_INVALID
+    assert binding.lib.attn_bwd_deterministic(None, None) == binding.ATTN_ERR_INVALID
     assert binding.lib.attn_bwd_workspace_size(None) == 0
 
 
@@ -128,21 +129,24 @@ def test_empty_problem_is_a_no_op(binding, shape):
     bp = binding.BwdParams()
     bp.fwd = p
     assert binding.lib.attn_bwd(ctypes.byref(bp), None) == binding.ATTN_OK
+    assert binding.lib.attn_bwd_deterministic(ctypes.byref(bp), None) == binding.ATTN_OK
     assert binding.lib.attn_bwd_workspace_size(ctypes.byref(p)) == 0
 
 
-def test_bwd_argument_errors(binding):
+@pytest.mark.parametrize("entry", ["attn_bwd", "attn_bwd_deterministic"])
+def test_bwd_argument_errors(binding, entry):
+    call = getattr(binding.lib, entry)
     bp = binding.BwdParams()
     bp.fwd = _params(binding, dtype=binding.ATTN_F32)
-    assert binding.lib.attn_bwd(ctypes.byref(bp), None) == binding.ATTN_ERR_UNSUPPORTED
+    assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_UNSUPPORTED
     bp.fwd = _params(binding)
-    assert binding.lib.attn_bwd(ctypes.byref(bp), None) == binding.ATTN_ERR_INVALID  # dout NULL
+    assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_INVALID  # dout NULL
     fake = 1 << 20
     st = (ctypes.c_int64 * 3)(128 * 64, 128 * 64, 64)
     bp.dout, bp.dq, bp.dk, bp.dv = fake, fake, fake, fake
     bp.do_stride, bp.dq_stride, bp.dk_stride, bp.dv_stride = st, st, st, st
     bp.workspace, bp.workspace_bytes = fake, 16
-    assert binding.lib.attn_bwd(ctypes.byref(bp), None) == binding.ATTN_ERR_WORKSPACE
+    assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_WORKSPACE
     assert "needed" in binding.last_error()
 
 

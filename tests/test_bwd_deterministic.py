@@ -1,0 +1,162 @@
+"""attn_bwd_deterministic: the backward pass whose dQ is summed over key tiles
+in a fixed order by a query-stationary kernel. Its gradients are checked
+against the fp64 oracle like attn_bwd's, and against themselves bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import ref
+from parity_util import assert_close_bf16, assert_grad, padded_mask, to64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def A():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import attn_fwd_03_gb300 as m
+    return m
+
+
+def _dev(x):
+    if x is None:
+        return None
+    if x.dim() == 4 and x.shape[-1] == x.shape[-2] and x.shape[-1] % 8 != 0:  # a mask: keep rows 16-byte aligned
+        return padded_mask(x, device="cuda")
+    return x.to("cuda")
+
+
+def _run(A, inp, causal, scale, entry="attn_bwd_deterministic"):
+    q, k, v, mask, do = (_dev(inp.get(n)) for n in ("q", "k", "v", "mask", "do"))
+    o, lse = A.attn_fwd(q, k, v, scale=scale, causal=causal, mask=mask)
+    grads = getattr(A, entry)(q, k, v, o, lse, do, scale=scale, causal=causal, mask=mask)
+    torch.cuda.synchronize()
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    return grads
+
+
+def _check(grads, inp, causal, scale):
+    mask = inp.get("mask")
+    args = (to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), to64(inp["do"]), scale, causal,
+            None if mask is None else to64(mask))
+    stored = ref.attention_backward(*args, o_storage="f16" if inp["q"].dtype == torch.float16 else "bf16")
+    pure = ref.attention_backward(*args)
+    for i, (name, g) in enumerate(zip(("dQ", "dK", "dV"), grads)):
+        assert_grad(name, g, pure[i], stored[i])
+
+
+def _inputs(shape, seed, dtype=torch.bfloat16):
+    return {n: W.random_tensor(shape, seed + i, dtype) for i, n in enumerate(("q", "k", "v", "do"))}
+
+
+@pytest.mark.parametrize("idx,shape", [
+    (2, (2, 3, 300, 64)),
+    (4, (2, 2, 520, 128)),
+    (5, (1, 2, 777, 128)),
+])
+def test_reduced_workloads(A, idx, shape):
+    w = W.WORKLOADS[idx]
+    inp = W.make_inputs(w, with_grad=True, shape=shape)
+    _check(_run(A, inp, w.causal, w.scale), inp, w.causal, w.scale)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 127, 129, 257])
+@pytest.mark.parametrize("causal", [False, True])
+def test_edge_lengths(A, d, N, causal):
+    inp = _inputs((1, 2, N, d), 1500)
+    scale = 1 / math.sqrt(d)
+    _check(_run(A, inp, causal, scale), inp, causal, scale)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_several_units_per_cta(A, d, causal):
+    # 2 x 12 heads x 8 query tiles = 192 units, more than one per SM: persistent CTAs carry
+    # barrier phases, tensor-memory buffers and the dQ accumulator across units
+    inp = _inputs((2, 12, 1024, d), 1600)
+    scale = 1 / math.sqrt(d)
+    _check(_run(A, inp, causal, scale), inp, causal, scale)
+
+
+def test_additive_mask_with_masked_rows(A):
+    B, H, N, d = 2, 2, 300, 128
+    inp = _inputs((B, H, N, d), 1700)
+    g = torch.Generator().manual_seed(17)
+    mask = torch.randn(B, H, N, N, generator=g) * 2
+    mask[torch.rand(mask.shape, generator=g) < 0.2] = float("-inf")
+    mask[:, :, 5, :] = float("-inf")
+    mask[:, :, 299, :] = float("-inf")
+    inp["mask"] = mask.to(torch.bfloat16)
+    for causal in (False, True):
+        dq, dk, dv = _run(A, inp, causal, 0.1)
+        _check((dq, dk, dv), inp, causal, 0.1)
+        assert torch.all(dq[:, :, 5] == 0) and torch.all(dq[:, :, 299] == 0)
+
+
+def test_fp16(A):
+    inp = _inputs((2, 2, 333, 64), 1800, torch.float16)
+    _check(_run(A, inp, True, 0.125), inp, True, 0.125)
+
+
+def test_all_rows_masked(A):
+    inp = _inputs((1, 1, 130, 64), 1900)
+    inp["mask"] = torch.full((1, 1, 130, 130), float("-inf"), dtype=torch.bfloat16)
+    dq, dk, dv = _run(A, inp, False, 0.125)
+    assert torch.all(dq == 0) and torch.all(dk == 0) and torch.all(dv == 0)
+
+
+def test_same_bits_every_call_and_agrees_with_attn_bwd(A):
+    inp = _inputs((2, 6, 1000, 64), 2000)
+    first = _run(A, inp, True, 0.125)
+    other = _inputs((1, 3, 400, 128), 2100)
+    _run(A, other, False, 0.09)  # a different problem in between
+    again = _run(A, inp, True, 0.125)
+    for name, a, b in zip(("dQ", "dK", "dV"), first, again):
+        assert torch.equal(a, b), name
+    atomic = _run(A, inp, True, 0.125, entry="attn_bwd")
+    # dK and dV come from the same kernel; dQ sums the same terms in another order
+    assert torch.equal(first[1], atomic[1]) and torch.equal(first[2], atomic[2])
+    assert_close_bf16("dQ vs attn_bwd", first[0], atomic[0].double().cpu().numpy(), relative_max=True)
+
+
+def test_poisoned_dq_fully_written(A):
+    inp = _inputs((1, 3, 383, 128), 2200)
+    q, k, v, do = (_dev(inp[n]) for n in ("q", "k", "v", "do"))
+    o, lse = A.attn_fwd(q, k, v, causal=True)
+    dq = torch.full_like(q, float("nan"))
+    A.attn_bwd_deterministic(q, k, v, o, lse, do, causal=True, dq=dq)
+    torch.cuda.synchronize()
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    assert not torch.isnan(dq).any()
+
+
+def test_empty_problem(A):
+    q = torch.empty((0, 2, 128, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((0, 2, 128), dtype=torch.float32, device="cuda")
+    dq, dk, dv = A.attn_bwd_deterministic(q, q, q, q, lse, q)
+    assert dq.shape == q.shape
+
+
+@pytest.mark.parametrize("idx", [2, 4, 5])
+def test_full_size_sampled(A, idx):
+    w = W.WORKLOADS[idx]
+    inp = W.make_inputs(w)
+    dq, dk, dv = _run(A, inp, w.causal, w.scale)
+    b, h = w.B - 1, w.H // 2
+    r = np.random.default_rng(300 + idx)
+    rows = np.array(sorted(set(r.choice(w.N, size=48, replace=False).tolist()) | {0, w.N - 1, 127, 128}))
+    maskh = None if inp.get("mask") is None else to64(inp["mask"][b, 0])
+    hargs = (to64(inp["q"][b, h]), to64(inp["k"][b, h]), to64(inp["v"][b, h]), to64(inp["do"][b, h]), w.scale,
+             w.causal, maskh)
+    pure = ref.backward_head(*hargs, q_rows=rows, k_rows=rows)
+    stored = ref.backward_head(*hargs, q_rows=rows, k_rows=rows, o_storage="bf16")
+    for i, (name, g) in enumerate((("dQ", dq), ("dK", dk), ("dV", dv))):
+        assert_grad(name, g[b, h, rows], pure[i], stored[i])
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
