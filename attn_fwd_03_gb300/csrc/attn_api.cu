@@ -106,7 +106,10 @@ attn_status_t check_fwd(const attn_fwd_params* p, bool* empty) {
     if (p->reserved0 != 0) return fail(ATTN_ERR_INVALID, "reserved0 must be 0");
     if (!std::isfinite(p->scale) || !(p->scale > 0.f))
         return fail(ATTN_ERR_INVALID, "scale must be positive and finite");
-    if (p->d != 64 && p->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not built (64 or 128)", p->d);
+    if (p->d != 64 && p->d != 128 && p->d != 256)
+        return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not built (64, 128 or 256)", p->d);
+    if (p->d == 256 && p->dtype == ATTN_F32)
+        return fail(ATTN_ERR_UNSUPPORTED, "head dim 256 is built for bf16 and fp16 only");
     if (p->B > 65535 || p->H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B and H are limited to 65535");
     *empty = (p->B == 0 || p->H == 0 || p->N == 0);
     if (*empty) return ATTN_OK;
@@ -184,6 +187,11 @@ attn_status_t build_fwd_maps(const attn_fwd_params& p, FwdMaps* m) {
     if ((st = encode_h16_map(&m->k, "k", p.k, d, N, p.H, p.B, p.k_stride, 128, DT)) != ATTN_OK) return st;
     if ((st = encode_h16_map(&m->v, "v", p.v, d, N, p.H, p.B, p.v_stride, 128, DT)) != ATTN_OK) return st;
     if ((st = encode_h16_map(&m->o, "o", p.o, d, N, p.H, p.B, p.o_stride, 128, DT)) != ATTN_OK) return st;
+    if (p.d == 256) {
+        if ((st = encode_h16_map(&m->v32, "v", p.v, d, N, p.H, p.B, p.v_stride, 32, DT)) != ATTN_OK) return st;
+    } else {
+        m->v32 = m->v;  // unused below head dim 256
+    }
     if (p.mask) {
         const uint64_t hm = p.mask_stride[1] != 0 ? (uint64_t)p.H : 1;
         const uint64_t bm = p.mask_stride[0] != 0 ? (uint64_t)p.B : 1;
@@ -270,6 +278,7 @@ attn_status_t bwd_check_inputs(const attn_bwd_params* p, bool* empty) {
     attn_status_t st = check_fwd(&p->fwd, empty);
     if (st != ATTN_OK) return st;
     if (p->fwd.dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 and fp16 only");
+    if (p->fwd.d == 256) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for head dim 64 and 128");
     if (*empty) return ATTN_OK;
     if ((st = check_tensor("dout", p->dout, p->do_stride, 2, false)) != ATTN_OK) return st;
     if ((st = check_tensor("dq", p->dq, p->dq_stride, 2, false)) != ATTN_OK) return st;
@@ -321,7 +330,7 @@ attn_status_t attn_fwd(const attn_fwd_params* p, void* stream) {
     } else {
         FwdMaps maps;
         if ((st = build_fwd_maps(*p, &maps)) != ATTN_OK) return st;
-        e = launch_fwd_tc(*p, maps, lc, s);
+        e = p->d == 256 ? launch_fwd256(*p, maps, lc, s) : launch_fwd_tc(*p, maps, lc, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
     return ATTN_OK;
@@ -333,16 +342,9 @@ size_t attn_bwd_workspace_size(const attn_fwd_params* p) {
 }
 
 attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
-    if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
     bool empty = false;
-    attn_status_t st = check_fwd(&p->fwd, &empty);
-    if (st != ATTN_OK) return st;
-    if (p->fwd.dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 and fp16 only");
-    if (empty) return ATTN_OK;
-    if ((st = check_tensor("dout", p->dout, p->do_stride, 2, false)) != ATTN_OK) return st;
-    if ((st = check_tensor("dq", p->dq, p->dq_stride, 2, false)) != ATTN_OK) return st;
-    if ((st = check_tensor("dk", p->dk, p->dk_stride, 2, false)) != ATTN_OK) return st;
-    if ((st = check_tensor("dv", p->dv, p->dv_stride, 2, false)) != ATTN_OK) return st;
+    attn_status_t st = bwd_check_inputs(p, &empty);
+    if (st != ATTN_OK || empty) return st;
     const size_t need = bwd_workspace_bytes(p->fwd);
     if (!p->workspace || p->workspace_bytes < need)
         return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", p->workspace_bytes, need);

@@ -24,6 +24,7 @@ struct LaunchCommon {
 // Tensor maps for the tcgen05 forward (built by the host API).
 struct FwdMaps {
     CUtensorMap q, k, v, o, mask;
+    CUtensorMap v32;  // d = 256 only: V with 32-row boxes
 };
 
 // Tensor maps for the tcgen05 backward.
@@ -64,6 +65,9 @@ cudaError_t launch_decode(const attn_decode_params& p, const DecodeSplit& plan, 
 
 // attn_fwd_sm103.cu — tcgen05 forward (bf16).
 cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);
+
+// attn_fwd256.cu — tcgen05 forward for head dim 256 (bf16 / fp16).
+cudaError_t launch_fwd256(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);
 
 // attn_bwd_sm103.cu — tcgen05 backward main kernel (bf16).
 cudaError_t launch_bwd_tc(const attn_bwd_params& p, const BwdMaps& maps, const BwdWorkspace& ws,

@@ -440,7 +440,7 @@ def run_ours(args, w, rank, world, local_rank):
     if world == 1 and not args.no_all:
         peak = peaks["bf16_tflops"]
         table = {}
-        for idx, wk in {**W.WORKLOADS, **W.F16_WORKLOADS}.items():
+        for idx, wk in {**W.WORKLOADS, **W.F16_WORKLOADS, **W.D256_WORKLOADS}.items():
             r = measure_workload(A, wk, 10, 3, dev, flush)
             for key in ("fwd", "bwd", "bwd_deterministic"):
                 if f"{key}_tflops" in r and wk.dtype in ("bf16", "f16"):

@@ -75,7 +75,8 @@ typedef enum attn_dtype_t {
  * needed for the final weighted average").
  */
 typedef struct attn_fwd_params {
-    int32_t B, H, N, d;      /* batch, heads, sequence length, head dim (64 or 128) */
+    int32_t B, H, N, d;      /* batch, heads, sequence length, head dim: 64 or 128;
+                                256 for the bf16 / fp16 forward only */
     int32_t dtype;           /* attn_dtype_t of Q, K, V, O (and the mask) */
     int32_t causal;          /* 1: key j is masked for query i iff j > i (absolute
                                 positions, 0-based; same N for queries and keys) */
@@ -97,8 +98,8 @@ typedef struct attn_fwd_params {
 /*
  * Backward problem: dQ, dK, dV of sum(dO * O) for the forward described by
  * `fwd`, whose o and lse (as written by attn_fwd) are READ here. Recomputes
- * S and P tile by tile; no gradient flows to the mask. bf16 and fp16
- * (ATTN_F32 returns ATTN_ERR_UNSUPPORTED).
+ * S and P tile by tile; no gradient flows to the mask. bf16 and fp16 at
+ * head dim 64 or 128 (ATTN_F32 and head dim 256 return ATTN_ERR_UNSUPPORTED).
  */
 typedef struct attn_bwd_params {
     attn_fwd_params fwd;
@@ -114,7 +115,7 @@ typedef struct attn_bwd_params {
     size_t workspace_bytes;
 } attn_bwd_params;
 
-/* Forward pass (every dtype). */
+/* Forward pass (every dtype; head dim 256 with bf16 or fp16). */
 ATTN_API attn_status_t attn_fwd(const attn_fwd_params *p, void *stream);
 
 /* Bytes of workspace attn_bwd needs for this problem (0 for an empty one):

@@ -91,7 +91,8 @@ def _params(binding, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(d=96), "ATTN_ERR_UNSUPPORTED"),
-    (dict(d=256), "ATTN_ERR_UNSUPPORTED"),
+    (dict(d=512), "ATTN_ERR_UNSUPPORTED"),
+    (dict(d=256, dtype=1), "ATTN_ERR_UNSUPPORTED"),  # head dim 256: 16-bit inputs only
     (dict(B=-1), "ATTN_ERR_INVALID"),
     (dict(N=-5), "ATTN_ERR_INVALID"),
     (dict(dtype=7), "ATTN_ERR_INVALID"),
@@ -138,6 +139,8 @@ def test_bwd_argument_errors(binding, entry):
     call = getattr(binding.lib, entry)
     bp = binding.BwdParams()
     bp.fwd = _params(binding, dtype=binding.ATTN_F32)
+    assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_UNSUPPORTED
+    bp.fwd = _params(binding, d=256)  # the forward only, so far
     assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_UNSUPPORTED
     bp.fwd = _params(binding)
     assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_INVALID  # dout NULL
