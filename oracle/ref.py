@@ -89,6 +89,21 @@ def round_f16(x) -> np.ndarray:
 _STORAGE = {"bf16": round_bf16, "f16": round_f16}
 
 
+def decode_e4m3(codes) -> np.ndarray:
+    """8-bit E4M3 floating-point codes (the FP8 format of an FP8 forward pass, "What is
+    FlashAttention?", FAQ on FlashAttention-3) -> fp64, from the format's definition:
+    bit 7 sign, bits 6..3 a biased exponent (bias 7), bits 2..0 the fraction.
+      exponent 0:        (fraction / 8) * 2^-6            (zero and subnormals)
+      exponent 1..15:    (1 + fraction / 8) * 2^(e - 7)   (largest finite: 448)
+      exponent 15 with fraction 7: not a number; the format has no infinities."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    e = (c >> 3) & 0xF
+    f = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, f / 8.0 * 2.0 ** -6, (1.0 + f / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((e == 15) & (c & 7 == 7), np.nan, mag)
+    return np.where((c & 0x80) != 0, -mag, mag)
+
+
 def _mask_for_head(mask: Optional[np.ndarray], b: int, h: int) -> Optional[np.ndarray]:
     """mask has shape (Bm, Hm, N, N) with Bm in {1, B} and Hm in {1, H}."""
     if mask is None:
@@ -157,6 +172,19 @@ def attention_forward(q, k, v, scale: float, causal: bool = False, mask=None):
             o[b, h], lse[b, h] = forward_head(q[b, h], k[b, h], v[b, h], scale, causal,
                                               _mask_for_head(mask, b, h))
     return o, lse
+
+
+def attention_forward_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float, scale: float,
+                          causal: bool = False, mask=None):
+    """FP8 forward: Q, K, V arrive as E4M3 codes (uint8) with one descale factor per tensor, and
+    the values they stand for are code value x descale. What the forward computes is the plain
+    attention of those values ("What is FlashAttention?", FAQ: FlashAttention-3's FP8 forward
+    computes the same attention at lower precision), so this is attention_forward on the
+    decoded, descaled inputs, in fp64."""
+    q = decode_e4m3(q8) * float(q_descale)
+    k = decode_e4m3(k8) * float(k_descale)
+    v = decode_e4m3(v8) * float(v_descale)
+    return attention_forward(q, k, v, scale, causal, mask)
 
 
 def decode_forward(q, k, v, scale: float, causal: bool = False):

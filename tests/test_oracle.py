@@ -627,3 +627,45 @@ def test_merged_states_equal_the_whole_row():
     empty = online.RowState(4)
     e = online.merge_states(empty, online.RowState(4))
     assert np.isneginf(e.m) and e.l == 0 and np.all(e.result() == 0)
+
+
+# ------------------------------------------------------------------ FP8 (E4M3) forward
+def test_decode_e4m3_matches_torch_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    got = ref.decode_e4m3(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_decode_e4m3_closed_forms():
+    d = lambda c: float(ref.decode_e4m3(np.array([c], dtype=np.uint8))[0])  # noqa: E731
+    assert d(0x00) == 0.0 and math.copysign(1.0, d(0x80)) == -1.0
+    assert d(0x01) == 2.0 ** -9 and d(0x07) == 7 * 2.0 ** -9  # subnormals
+    assert d(0x08) == 2.0 ** -6  # smallest normal
+    assert d(0x38) == 1.0 and d(0x3C) == 1.5 and d(0x40) == 2.0 and d(0xB8) == -1.0
+    assert d(0x7E) == 448.0 and d(0xFE) == -448.0 and d(0x77) == 240.0
+    assert math.isnan(d(0x7F)) and math.isnan(d(0xFF))
+
+
+def test_fp8_forward_is_attention_of_the_values_the_codes_stand_for():
+    # codes 0x30..0x47 stand for 0.5 .. 3.75 in steps the bf16 format holds exactly, so the
+    # FP8 forward must equal the plain forward of those values times the descales
+    rng = np.random.default_rng(5)
+    shape = (1, 2, 37, 8)
+    q8, k8, v8 = (rng.integers(0x30, 0x48, size=shape).astype(np.uint8) for _ in range(3))
+    signs = [np.where(rng.random(shape) < 0.5, 0x80, 0).astype(np.uint8) for _ in range(3)]
+    q8, k8, v8 = q8 | signs[0], k8 | signs[1], v8 | signs[2]
+    qd, kd, vd = 0.25, 0.5, 2.0
+    for causal in (False, True):
+        o, lse = ref.attention_forward_fp8(q8, k8, v8, qd, kd, vd, 0.3, causal)
+        qv = torch.from_numpy(q8).view(torch.float8_e4m3fn).double() * qd
+        kv = torch.from_numpy(k8).view(torch.float8_e4m3fn).double() * kd
+        vv = torch.from_numpy(v8).view(torch.float8_e4m3fn).double() * vd
+        want = torch.nn.functional.scaled_dot_product_attention(qv, kv, vv, scale=0.3, is_causal=causal)
+        assert np.allclose(o, want.numpy(), rtol=0, atol=1e-13)
+        # a single key: O is that key's value row
+    o1, _ = ref.attention_forward_fp8(q8[:, :, :1], k8[:, :, :1], v8[:, :, :1], qd, kd, vd, 0.3)
+    assert np.array_equal(o1, ref.decode_e4m3(v8[:, :, :1]) * vd)
