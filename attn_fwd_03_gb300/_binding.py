@@ -27,6 +27,7 @@ ATTN_ERR_WORKSPACE = -6
 ATTN_BF16 = 0
 ATTN_F32 = 1
 ATTN_F16 = 2
+ATTN_E4M3 = 3
 
 STATUS_NAMES = {
     ATTN_OK: "ATTN_OK", ATTN_ERR_INVALID: "ATTN_ERR_INVALID", ATTN_ERR_UNSUPPORTED: "ATTN_ERR_UNSUPPORTED",
@@ -35,7 +36,7 @@ STATUS_NAMES = {
 }
 
 # every symbol include/attn.h declares
-EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_deterministic", "attn_bwd_workspace_size",
+EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_bwd", "attn_bwd_noalloc", "attn_bwd_deterministic", "attn_bwd_workspace_size",
             "attn_decode",
             "attn_decode_workspace_size", "attn_status", "attn_last_error",
             "attn_set_wait_timeout_ns", "attn_debug_set_producer_stall", "attn_debug_set_bwd_events",
@@ -66,6 +67,14 @@ class BwdParams(ctypes.Structure):
     ]
 
 
+class Fp8Params(ctypes.Structure):
+    _fields_ = [
+        ("f", FwdParams),
+        ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float), ("v_descale", ctypes.c_float),
+        ("reserved1", ctypes.c_int32),
+    ]
+
+
 class DecodeParams(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("nq", ctypes.c_int32), ("nk", ctypes.c_int32),
@@ -90,6 +99,8 @@ def _load() -> ctypes.CDLL:
     lib = ctypes.CDLL(LIB_PATH)
     lib.attn_fwd.argtypes = [ctypes.POINTER(FwdParams), ctypes.c_void_p]
     lib.attn_fwd.restype = ctypes.c_int
+    lib.attn_fwd_fp8.argtypes = [ctypes.POINTER(Fp8Params), ctypes.c_void_p]
+    lib.attn_fwd_fp8.restype = ctypes.c_int
     lib.attn_bwd.argtypes = [ctypes.POINTER(BwdParams), ctypes.c_void_p]
     lib.attn_bwd.restype = ctypes.c_int
     lib.attn_bwd_noalloc.argtypes = [ctypes.POINTER(BwdParams), ctypes.c_void_p]
@@ -141,6 +152,8 @@ def _dtype_code(t: torch.dtype) -> int:
         return ATTN_F32
     if t == torch.float16:
         return ATTN_F16
+    if t in (torch.float8_e4m3fn, torch.uint8):
+        return ATTN_E4M3
     raise TypeError(f"unsupported dtype {t}")
 
 
@@ -185,6 +198,27 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: Option
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     p = fwd_params(q, k, v, out, lse, scale, causal, mask)
     _check(lib.attn_fwd(ctypes.byref(p), ctypes.c_void_p(_stream_handle(stream))))
+    return out, lse
+
+
+def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, *,
+                 scale: Optional[float] = None, causal: bool = False, mask: Optional[torch.Tensor] = None,
+                 out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """FP8 forward: q, k, v are [B, H, N, 128] E4M3 tensors (torch.float8_e4m3fn, or
+    uint8 holding the codes) standing for code x descale; O is bf16, LSE fp32."""
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    p = Fp8Params()
+    p.f = fwd_params(q, k, v, out, lse, scale, causal, mask)
+    p.q_descale, p.k_descale, p.v_descale = float(q_descale), float(k_descale), float(v_descale)
+    p.reserved1 = 0
+    _check(lib.attn_fwd_fp8(ctypes.byref(p), ctypes.c_void_p(_stream_handle(stream))))
     return out, lse
 
 

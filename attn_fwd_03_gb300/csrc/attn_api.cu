@@ -100,6 +100,7 @@ attn_status_t check_fwd(const attn_fwd_params* p, bool* empty) {
     if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
     if (p->B < 0 || p->H < 0 || p->N < 0)
         return fail(ATTN_ERR_INVALID, "negative size B=%d H=%d N=%d", p->B, p->H, p->N);
+    if (p->dtype == ATTN_E4M3) return fail(ATTN_ERR_UNSUPPORTED, "E4M3 inputs go through attn_fwd_fp8");
     if (p->dtype != ATTN_BF16 && p->dtype != ATTN_F32 && p->dtype != ATTN_F16)
         return fail(ATTN_ERR_INVALID, "unknown dtype %d", p->dtype);
     if (p->causal != 0 && p->causal != 1) return fail(ATTN_ERR_INVALID, "causal must be 0 or 1, got %d", p->causal);
@@ -200,6 +201,67 @@ attn_status_t build_fwd_maps(const attn_fwd_params& p, FwdMaps* m) {
     } else {
         m->mask = m->q;  // unused by the kernel variant without a mask
     }
+    return ATTN_OK;
+}
+
+// 4-D map of E4M3 codes over (col, row, h, b) with 128 x 128 boxes and the 128-byte swizzle.
+attn_status_t encode_u8_map(CUtensorMap* m, const char* name, const void* base, uint64_t cols, uint64_t rows,
+                            uint64_t hs, uint64_t bs, const int64_t* st) {
+    cuuint64_t dims[4] = {cols, rows, hs, bs};
+    cuuint64_t strides[3] = {(cuuint64_t)st[2], (cuuint64_t)st[1], (cuuint64_t)st[0]};
+    for (int i = 0; i < 3; ++i)
+        if (strides[i] == 0) strides[i] = 16;
+    cuuint32_t box[4] = {128, 128, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", name, (int)r);
+    return ATTN_OK;
+}
+
+attn_status_t check_fwd_fp8(const attn_fwd_fp8_params* p, bool* empty) {
+    if (!p) return fail(ATTN_ERR_INVALID, "params is NULL");
+    const attn_fwd_params& f = p->f;
+    if (f.B < 0 || f.H < 0 || f.N < 0) return fail(ATTN_ERR_INVALID, "negative size B=%d H=%d N=%d", f.B, f.H, f.N);
+    if (f.dtype != ATTN_E4M3) return fail(ATTN_ERR_UNSUPPORTED, "attn_fwd_fp8 takes ATTN_E4M3 inputs, got %d", f.dtype);
+    if (f.causal != 0 && f.causal != 1) return fail(ATTN_ERR_INVALID, "causal must be 0 or 1, got %d", f.causal);
+    if (f.reserved0 != 0 || p->reserved1 != 0) return fail(ATTN_ERR_INVALID, "reserved fields must be 0");
+    if (!std::isfinite(f.scale) || !(f.scale > 0.f)) return fail(ATTN_ERR_INVALID, "scale must be positive and finite");
+    const float ds[3] = {p->q_descale, p->k_descale, p->v_descale};
+    for (int i = 0; i < 3; ++i)
+        if (!std::isfinite(ds[i]) || !(ds[i] > 0.f))
+            return fail(ATTN_ERR_INVALID, "descale factors must be positive and finite");
+    if (f.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward is built for head dim 128, got %d", f.d);
+    if (f.B > 65535 || f.H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B and H are limited to 65535");
+    *empty = (f.B == 0 || f.H == 0 || f.N == 0);
+    if (*empty) return ATTN_OK;
+    attn_status_t st;
+    if ((st = check_tensor("q", f.q, f.q_stride, 1, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("k", f.k, f.k_stride, 1, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("v", f.v, f.v_stride, 1, false)) != ATTN_OK) return st;
+    if ((st = check_tensor("o", f.o, f.o_stride, 2, false)) != ATTN_OK) return st;
+    if (!f.lse) return fail(ATTN_ERR_INVALID, "lse is NULL");
+    if (misaligned_ptr(f.lse)) return fail(ATTN_ERR_ALIGN, "lse is not 16-byte aligned");
+    if (f.mask && (st = check_tensor("mask", f.mask, f.mask_stride, 2, true)) != ATTN_OK) return st;
+    if (f.mask && f.mask_stride[2] == 0 && f.N > 1) return fail(ATTN_ERR_INVALID, "mask row stride must be positive");
+    return ATTN_OK;
+}
+
+attn_status_t build_fp8_maps(const attn_fwd_fp8_params& p, Fp8Maps* m) {
+    attn_status_t st = get_encoder();
+    if (st != ATTN_OK) return st;
+    const attn_fwd_params& f = p.f;
+    const uint64_t N = (uint64_t)f.N, d = (uint64_t)f.d;
+    if ((st = encode_u8_map(&m->q, "q", f.q, d, N, f.H, f.B, f.q_stride)) != ATTN_OK) return st;
+    if ((st = encode_u8_map(&m->k, "k", f.k, d, N, f.H, f.B, f.k_stride)) != ATTN_OK) return st;
+    if ((st = encode_u8_map(&m->v, "v", f.v, d, N, f.H, f.B, f.v_stride)) != ATTN_OK) return st;
+    if (f.mask) {
+        const uint64_t hm = f.mask_stride[1] != 0 ? (uint64_t)f.H : 1;
+        const uint64_t bm = f.mask_stride[0] != 0 ? (uint64_t)f.B : 1;
+        return encode_h16_map(&m->mask, "mask", f.mask, N, N, hm, bm, f.mask_stride, 128, ATTN_BF16);
+    }
+    m->mask = m->q;  // unused by the kernel variant without a mask
     return ATTN_OK;
 }
 
@@ -333,6 +395,19 @@ attn_status_t attn_fwd(const attn_fwd_params* p, void* stream) {
         e = p->d == 256 ? launch_fwd256(*p, maps, lc, s) : launch_fwd_tc(*p, maps, lc, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "attn_fwd launch");
+    return ATTN_OK;
+}
+
+attn_status_t attn_fwd_fp8(const attn_fwd_fp8_params* p, void* stream) {
+    bool empty = false;
+    attn_status_t st = check_fwd_fp8(p, &empty);
+    if (st != ATTN_OK || empty) return st;
+    LaunchCommon lc;
+    if ((st = device_setup(&lc)) != ATTN_OK) return st;
+    Fp8Maps maps;
+    if ((st = build_fp8_maps(*p, &maps)) != ATTN_OK) return st;
+    const cudaError_t e = launch_fwd_fp8(*p, maps, lc, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_fp8 launch");
     return ATTN_OK;
 }
 

@@ -245,6 +245,36 @@ def measure_workload(A, w, steps, warmup, dev, flush):
             out[f"{key}_tflops"] = 2.5 * f / (res[key] * 1e-3) / 1e12
     return out
 
+def measure_fp8(A, w, steps, warmup, dev, flush):
+    """FP8 forward milliseconds of one E4M3 workload (CUDA events on the launching stream, L2
+    rewritten before every timed call). TFLOP/s counts the same 4 B H N^2 d (halved for causal)
+    as the 16-bit forward; the percentage is of the measured bf16 dense peak times the nominal
+    E4M3 / bf16 tensor-rate ratio of 2."""
+    import torch
+    inp = W.make_fp8_inputs(w)
+    q, k, v = (inp[n].to(dev).view(torch.float8_e4m3fn) for n in ("q8", "k8", "v8"))
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    fn = lambda: A.attn_fwd_fp8(q, k, v, inp["q_ds"], inp["k_ds"], inp["v_ds"], scale=w.scale,  # noqa: E731
+                                causal=w.causal, out=o, lse=lse)
+    for _ in range(warmup):
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        flush.fill_(3)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if A.attn_status() != A.ATTN_OK:
+        raise RuntimeError(A.last_error())
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+    f = W.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    return {"shape": [w.B, w.H, w.N, w.d], "dtype": "e4m3", "causal": w.causal, "mask": w.mask, "fwd_ms": ms,
+            "fwd_tflops": f / (ms * 1e-3) / 1e12}
+
+
 def run_ours(args, w, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -445,6 +475,10 @@ def run_ours(args, w, rank, world, local_rank):
             for key in ("fwd", "bwd", "bwd_deterministic"):
                 if f"{key}_tflops" in r and wk.dtype in ("bf16", "f16"):
                     r[f"{key}_pct_of_peak"] = 100.0 * r[f"{key}_tflops"] / peak
+            table[wk.name] = r
+        for idx, wk in W.FP8_WORKLOADS.items():
+            r = measure_fp8(A, wk, 10, 3, dev, flush)
+            r["fwd_pct_of_e4m3_peak"] = 100.0 * r["fwd_tflops"] / (2.0 * peak)
             table[wk.name] = r
         for nq in (1, 8):
             table[f"decode_b8_h32_nq{nq}_nk8192_d128_bf16_causal"] = measure_decode(A, dev, peaks["hbm_gbs"], nq)

@@ -64,8 +64,10 @@ typedef enum attn_status_t {
 typedef enum attn_dtype_t {
     ATTN_BF16 = 0, /* bfloat16 storage, fp32 accumulation (tcgen05 tensor cores) */
     ATTN_F32 = 1,  /* float32 storage and arithmetic (CUDA cores; forward only)   */
-    ATTN_F16 = 2   /* IEEE half storage, fp32 accumulation (tcgen05 tensor cores);
+    ATTN_F16 = 2,  /* IEEE half storage, fp32 accumulation (tcgen05 tensor cores);
                       P, dS and O are rounded to half as bf16 rounds them for bf16 */
+    ATTN_E4M3 = 3  /* 8-bit E4M3 Q, K, V with per-tensor descale factors; the FP8
+                      forward (attn_fwd_fp8) only, whose O is bf16 */
 } attn_dtype_t;
 
 /*
@@ -117,6 +119,31 @@ typedef struct attn_bwd_params {
 
 /* Forward pass (every dtype; head dim 256 with bf16 or fp16). */
 ATTN_API attn_status_t attn_fwd(const attn_fwd_params *p, void *stream);
+
+/*
+ * FP8 forward problem ("What is FlashAttention?", FAQ: FlashAttention-3 has
+ * an FP8 forward pass). Q, K and V hold E4M3 codes, one byte per element
+ * (sign, 4 exponent bits with bias 7, 3 fraction bits, no infinities), and
+ * stand for code value x descale. The result is the attention of those
+ * values, as attn_fwd defines it, with the products on the 8-bit tensor
+ * cores and P rounded to E4M3 before it multiplies V.
+ *  - f.dtype = ATTN_E4M3; f.d = 128. q, k, v strides count bytes (elements)
+ *    and must be multiples of 16. f.o is bf16 [B, H, N, d] (strides in bf16
+ *    elements); f.mask, when given, is bf16 as for attn_fwd; f.lse as attn_fwd.
+ *  - Accuracy: each probability carries up to 2^-4 relative rounding, so O
+ *    differs from the exact attention of the decoded inputs by at most
+ *    2^-4 x max|v| per element (plus bf16 output rounding), and typically by
+ *    1-3 % in relative L2 norm.
+ */
+typedef struct attn_fwd_fp8_params {
+    attn_fwd_params f;
+    float q_descale, k_descale, v_descale;  /* finite and > 0 */
+    int32_t reserved1;                      /* must be 0 */
+} attn_fwd_fp8_params;
+
+/* FP8 forward pass (tcgen05 kind::f8f6f4). Same conventions and errors as
+ * attn_fwd; a 16-bit dtype here, or E4M3 given to attn_fwd, is rejected. */
+ATTN_API attn_status_t attn_fwd_fp8(const attn_fwd_fp8_params *p, void *stream);
 
 /* Bytes of workspace attn_bwd needs for this problem (0 for an empty one):
  * per (b, h) and 128-row query tile 1 KiB of fp32 row statistics

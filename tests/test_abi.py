@@ -53,10 +53,12 @@ def test_struct_layout_matches_c(binding):
 #include <stddef.h>
 #include "attn.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(attn_fwd_params), offsetof(attn_fwd_params, q),
-         offsetof(attn_fwd_params, mask_stride), sizeof(attn_bwd_params), offsetof(attn_bwd_params, dout),
-         offsetof(attn_bwd_params, workspace_bytes), sizeof(attn_decode_params), offsetof(attn_decode_params, q),
-         offsetof(attn_decode_params, num_splits), offsetof(attn_decode_params, workspace_bytes));
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(attn_fwd_params),
+         offsetof(attn_fwd_params, q), offsetof(attn_fwd_params, mask_stride), sizeof(attn_bwd_params),
+         offsetof(attn_bwd_params, dout), offsetof(attn_bwd_params, workspace_bytes), sizeof(attn_decode_params),
+         offsetof(attn_decode_params, q), offsetof(attn_decode_params, num_splits),
+         offsetof(attn_decode_params, workspace_bytes), sizeof(attn_fwd_fp8_params),
+         offsetof(attn_fwd_fp8_params, q_descale), offsetof(attn_fwd_fp8_params, reserved1));
   return 0;
 }
 '''
@@ -66,10 +68,10 @@ int main(void) {
         open(c, "w").write(src)
         subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
         got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
-    F, B, Dp = binding.FwdParams, binding.BwdParams, binding.DecodeParams
+    F, B, Dp, F8 = binding.FwdParams, binding.BwdParams, binding.DecodeParams, binding.Fp8Params
     want = [ctypes.sizeof(F), F.q.offset, F.mask_stride.offset, ctypes.sizeof(B), B.dout.offset,
             B.workspace_bytes.offset, ctypes.sizeof(Dp), Dp.q.offset, Dp.num_splits.offset,
-            Dp.workspace_bytes.offset]
+            Dp.workspace_bytes.offset, ctypes.sizeof(F8), F8.q_descale.offset, F8.reserved1.offset]
     assert got == want
 
 
@@ -214,3 +216,36 @@ def test_decode_empty_problem_is_a_no_op(binding, shape):
     B, H, nq = shape
     p = _decode_params(binding, B=B, H=H, nq=nq, q=0, k=0, v=0, o=0, lse=0)
     assert binding.lib.attn_decode(ctypes.byref(p), None) == binding.ATTN_OK
+
+
+def _fp8_params(binding, **kw):
+    p = binding.Fp8Params()
+    p.f = _params(binding, **{"d": 128, "dtype": binding.ATTN_E4M3, "stride": (128 * 128, 128 * 128, 128), **kw})
+    p.q_descale, p.k_descale, p.v_descale = kw.get("descale", (0.5, 0.5, 0.5))
+    p.reserved1 = kw.get("reserved1", 0)
+    return p
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=64), "ATTN_ERR_UNSUPPORTED"),
+    (dict(dtype=0), "ATTN_ERR_UNSUPPORTED"),  # a 16-bit dtype goes through attn_fwd
+    (dict(descale=(0.5, 0.0, 0.5)), "ATTN_ERR_INVALID"),
+    (dict(descale=(0.5, 0.5, float("inf"))), "ATTN_ERR_INVALID"),
+    (dict(reserved1=3), "ATTN_ERR_INVALID"),
+    (dict(causal=2), "ATTN_ERR_INVALID"),
+    (dict(N=-1), "ATTN_ERR_INVALID"),
+    (dict(stride=(128 * 128, 128 * 128, 120)), "ATTN_ERR_ALIGN"),  # rows of 120 bytes
+])
+def test_fp8_argument_errors(binding, kw, status):
+    p = _fp8_params(binding, **kw)
+    assert binding.lib.attn_fwd_fp8(ctypes.byref(p), None) == getattr(binding, status)
+    assert binding.last_error()
+
+
+def test_fp8_null_and_empty(binding):
+    assert binding.lib.attn_fwd_fp8(None, None) == binding.ATTN_ERR_INVALID
+    p = _fp8_params(binding, B=0)
+    assert binding.lib.attn_fwd_fp8(ctypes.byref(p), None) == binding.ATTN_OK
+    # E4M3 given to the 16-bit entry point is refused
+    f = _params(binding, d=128, dtype=binding.ATTN_E4M3)
+    assert binding.lib.attn_fwd(ctypes.byref(f), None) == binding.ATTN_ERR_UNSUPPORTED

@@ -40,7 +40,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str  # "bf16", "f16" or "f32"
+    dtype: str  # "bf16", "f16", "f32" or "e4m3"
     causal: bool
     mask: bool
     backward: bool
@@ -146,6 +146,40 @@ def make_inputs(w: Workload, with_grad: Optional[bool] = None, shape=None) -> Di
     if w.mask:
         ws = dataclasses.replace(w, B=B, N=N)
         out["mask"] = make_mask(ws)
+    return out
+
+
+# FP8 forward (E4M3 inputs, "What is FlashAttention?", FAQ on FlashAttention-3): the
+# d = 128 layer shape and the long causal context, forward only.
+FP8_WORKLOADS: Dict[int, Workload] = {
+    9: Workload(9, "b1_h32_n8192_d128_e4m3_fwd", 1, 32, 8192, 128, "e4m3", False, False, False),
+    10: Workload(10, "b1_h16_n32768_d128_e4m3_causal_fwd", 1, 16, 32768, 128, "e4m3", True, False, False),
+}
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """fp32 tensor -> (E4M3 codes as uint8, descale) with one per-tensor factor,
+    descale = max|x| / 448 (448 is E4M3's largest finite value), so code x descale
+    approximates x. Rounding is torch's float8_e4m3fn conversion."""
+    amax = float(x.abs().max()) if x.numel() else 1.0
+    # an fp32 value, as the library takes it
+    descale = float(torch.tensor(amax / 448.0 if amax > 0 else 1.0, dtype=torch.float32))
+    codes = (x / descale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, descale
+
+
+def make_fp8_inputs(w: Workload, shape=None) -> Dict[str, object]:
+    """E4M3 codes q8, k8, v8 (uint8, CPU) and their descales q_ds, k_ds, v_ds, from the same
+    N(0, 1) draws (seeds 1000+k, 2000+k, 3000+k) as make_inputs."""
+    B, H, N, d = shape if shape is not None else (w.B, w.H, w.N, w.d)
+    out: Dict[str, object] = {}
+    for name, seed in (("q", 1000), ("k", 2000), ("v", 3000)):
+        x = _normal((B, H, N, d), seed + w.index)
+        if name in ("q", "k") and w.qk_mult != 1.0:
+            x = x * w.qk_mult
+        out[name + "8"], out[name + "_ds"] = quantize_e4m3(x)
+    if w.mask:
+        out["mask"] = make_mask(dataclasses.replace(w, B=B, N=N, dtype="bf16"))
     return out
 
 
