@@ -93,7 +93,7 @@ struct FwdCfg {
     static constexpr int kKVOff = kQOff + 2 * kTileBytes;
     static constexpr int kMaskOff = kKVOff + kStages * kTileBytes;
     static constexpr int kBarOff = kMaskOff + (MASK ? 2 * kMaskBytes : 0);
-    static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
+    static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + alignment slack
 };
 
 struct FwdParamsDev {
@@ -121,6 +121,7 @@ struct __align__(8) Barriers {
     uint32_t tmem_base;
     int abort_flag;
 };
+static_assert(sizeof(Barriers) <= 512, "barrier area");
 
 struct Unit {
     int b, h, qblk;
