@@ -78,12 +78,14 @@ __device__ __forceinline__ float finish_score(float dot, const SimtArgs& a, int 
 }
 
 // ------------------------------------------------------------------ forward
-// Block: 4 warps, 32 query rows (8 per warp). Key tiles of 32 keys staged in
+// Block: 4 warps, 8 query rows (2 per warp), so even a single head of a few
+// hundred rows spreads over dozens of SMs. Key tiles of 32 keys staged in
 // shared memory; lane j scores key j of the tile for one row at a time, the
 // row's (m, l) live in every lane, lane owns output dims lane + 32 t.
+constexpr int kSimtRows = 8;
 template <typename T, int D>
 __global__ void __launch_bounds__(128) fwd_simt_kernel(SimtArgs a) {
-    constexpr int BR = 32, BC = 32, RPW = 8, DT = D / 32;
+    constexpr int BR = kSimtRows, BC = 32, RPW = BR / 4, DT = D / 32;
     extern __shared__ float sm[];
     float(*Qs)[D] = reinterpret_cast<float(*)[D]>(sm);
     float(*Ks)[D + 1] = reinterpret_cast<float(*)[D + 1]>(sm + BR * D);
@@ -304,10 +306,10 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 template <typename T, int D>
 cudaError_t fwd_simt_launch(const SimtArgs& a, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (32 * D + 32 * (D + 1) + 32 * D);
+    const size_t smem = sizeof(float) * (kSimtRows * D + 32 * (D + 1) + 32 * D);
     cudaError_t e = set_smem(fwd_simt_kernel<T, D>, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((a.N + 31) / 32, a.H, a.B);
+    dim3 grid((a.N + kSimtRows - 1) / kSimtRows, a.H, a.B);
     fwd_simt_kernel<T, D><<<grid, 128, smem, s>>>(a);
     return cudaGetLastError();
 }

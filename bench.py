@@ -545,6 +545,26 @@ def captured_traffic(kernel: str, workload: str):
     return None
 
 
+def run_table_entry(args):
+    """One row of the per-workload table, timed alone on GPU 0 (--steps timed calls after
+    --warmup, L2 rewritten before each)."""
+    import torch
+    import attn_fwd_03_gb300 as A
+    every = {**W.WORKLOADS, **W.F16_WORKLOADS, **W.D256_WORKLOADS, **W.FP8_WORKLOADS}
+    by_name = {wk.name: wk for wk in every.values()}
+    if args.table_workload not in by_name:
+        raise SystemExit(f"unknown workload {args.table_workload}; one of {sorted(by_name)}")
+    wk = by_name[args.table_workload]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    if wk.dtype == "e4m3":
+        r = measure_fp8(A, wk, args.steps, args.warmup, dev, flush)
+    else:
+        r = measure_workload(A, wk, args.steps, args.warmup, dev, flush)
+    print(json.dumps({"workload": wk.name, **r}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -556,12 +576,18 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-all", action="store_true", help="skip the per-workload forward/backward table")
+    ap.add_argument("--table-workload", default=None,
+                    help="time only this entry of the per-workload table (a workload name from workloads.py, "
+                         "e.g. under a profiler) and print it as one JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.table_workload is not None:
+        run_table_entry(args)
+        return
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w, rank, world)

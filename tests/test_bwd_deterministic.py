@@ -160,3 +160,15 @@ def test_full_size_sampled(A, idx):
         assert_grad(name, g[b, h, rows], pure[i], stored[i])
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()
+
+
+def test_bnhd_strided_layout(A):
+    inp = _inputs((2, 300, 3, 64), 2300)  # stored [B, N, H, d]
+    view = {n: x.cuda().permute(0, 2, 1, 3) for n, x in inp.items()}
+    o, lse = A.attn_fwd(view["q"], view["k"], view["v"], scale=0.125, causal=True)
+    grads = [torch.empty((2, 300, 3, 64), dtype=torch.bfloat16, device="cuda").permute(0, 2, 1, 3) for _ in range(3)]
+    A.attn_bwd_deterministic(view["q"], view["k"], view["v"], o, lse, view["do"], scale=0.125, causal=True,
+                             dq=grads[0], dk=grads[1], dv=grads[2])
+    torch.cuda.synchronize()
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    _check(grads, {n: x.permute(0, 2, 1, 3) for n, x in inp.items()}, True, 0.125)

@@ -118,3 +118,14 @@ def test_full_size_sampled(A, idx):
                                 None, rows=rows)
         assert_close_bf16(f"O[{b},{h}]", o[b, h, rows], O)
         assert_lse(lse[b, h, rows], L)
+
+
+def test_bnhd_strided_layout(A):
+    # [B, N, H, d] storage seen as [B, H, N, d] views: row stride H * d
+    inp = _inputs((2, 3, 200, 256), 3800)
+    q, k, v = (x.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3) for x in (inp["q"], inp["k"], inp["v"]))
+    o = torch.empty((2, 200, 3, 256), dtype=torch.bfloat16, device="cuda").permute(0, 2, 1, 3)
+    A.attn_fwd(q, k, v, scale=1 / 16, causal=True, out=o)
+    torch.cuda.synchronize()
+    O, _ = ref.attention_forward(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), 1 / 16, True)
+    assert_close_bf16("O", o, O)

@@ -169,3 +169,15 @@ def test_full_size_sampled(A, idx):
     rows = np.array(sorted(set(r.choice(w.N, size=32, replace=False).tolist()) | {0, w.N - 1, 127, 128}))
     res = _bound_and_ref(inp, w.scale, w.causal, None, heads=[(0, 0), (w.B - 1, w.H - 1)], rows=rows)
     _check(o, lse, res, rows=rows)
+
+
+def test_bnhd_strided_layout(A):
+    inp = _inputs((2, 3, 300, 128), 4700)
+    dev = lambda t: t.permute(0, 2, 1, 3).contiguous().cuda().permute(0, 2, 1, 3).view(torch.float8_e4m3fn)  # noqa: E731
+    o = torch.empty((2, 300, 3, 128), dtype=torch.bfloat16, device="cuda").permute(0, 2, 1, 3)
+    lse = torch.empty((2, 3, 300), dtype=torch.float32, device="cuda")
+    A.attn_fwd_fp8(dev(inp["q8"]), dev(inp["k8"]), dev(inp["v8"]), inp["q_ds"], inp["k_ds"], inp["v_ds"],
+                   scale=0.1, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    _check(o, lse, _bound_and_ref(inp, 0.1, True, None))
