@@ -4,7 +4,7 @@ thin Python binding.
     from attn_fwd_03_gb300 import attn_fwd, attn_bwd
     o, lse = attn_fwd(q, k, v, causal=True)            # q, k, v: [B, H, N, d] on cuda
     dq, dk, dv = attn_bwd(q, k, v, o, lse, do, causal=True)
-    o1, lse1 = attn_decode(q1, k_cache, v_cache, causal=True)  # q1: [B, H, nq <= 16, d]
+    o1, lse1 = attn_decode(q1, k_cache, v_cache, causal=True)  # q1: [B, H, nq <= 128, d]
     o8, lse8 = attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale)  # E4M3 inputs, d = 128
 
 The kernels live in csrc/ (built in-tree by build.py); the public C header is

@@ -300,7 +300,7 @@ def decode_workspace_size(q, k, v, *, causal: bool = False, num_splits: int = 0)
 
 def attn_decode(q, k, v, *, scale: Optional[float] = None, causal: bool = False, out=None, lse=None,
                 workspace=None, num_splits: int = 0, stream=None):
-    """Split-KV decode: q [B, H, nq <= 16, d] against k, v [B, H, nk, d]. With causal the
+    """Split-KV decode: q [B, H, nq <= 128, d] against k, v [B, H, nk, d]. With causal the
     queries are the last nq positions. Returns (O, LSE)."""
     B, H, nq, d = q.shape
     if scale is None:

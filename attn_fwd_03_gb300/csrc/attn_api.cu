@@ -279,7 +279,7 @@ attn_status_t check_decode(const attn_decode_params* p, bool* empty) {
     if (!std::isfinite(p->scale) || !(p->scale > 0.f))
         return fail(ATTN_ERR_INVALID, "scale must be positive and finite");
     if (p->d != 64 && p->d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not built (64 or 128)", p->d);
-    if (p->nq > 16) return fail(ATTN_ERR_UNSUPPORTED, "decode takes at most 16 query rows, got %d", p->nq);
+    if (p->nq > 128) return fail(ATTN_ERR_UNSUPPORTED, "decode takes at most 128 query rows, got %d", p->nq);
     if ((long long)p->B * p->H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B * H is limited to 65535");
     *empty = (p->B == 0 || p->H == 0 || p->nq == 0);
     if (*empty) return ATTN_OK;
@@ -492,7 +492,19 @@ attn_status_t attn_decode(const attn_decode_params* p, void* stream) {
     if (p->workspace_bytes < plan.workspace_bytes)
         return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", p->workspace_bytes,
                     plan.workspace_bytes);
-    cudaError_t e = launch_decode(*p, plan, static_cast<cudaStream_t>(stream));
+    DecodeMaps maps;
+    if ((st = get_encoder()) != ATTN_OK) return st;
+    const uint64_t d = (uint64_t)p->d;
+    if ((st = encode_h16_map(&maps.q, "q", p->q, d, (uint64_t)p->nq, p->H, p->B, p->q_stride, 128, p->dtype)) !=
+        ATTN_OK)
+        return st;
+    if ((st = encode_h16_map(&maps.k, "k", p->k, d, (uint64_t)p->nk, p->H, p->B, p->k_stride, 128, p->dtype)) !=
+        ATTN_OK)
+        return st;
+    if ((st = encode_h16_map(&maps.v, "v", p->v, d, (uint64_t)p->nk, p->H, p->B, p->v_stride, 128, p->dtype)) !=
+        ATTN_OK)
+        return st;
+    cudaError_t e = launch_decode(*p, plan, maps, lc, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_decode launch");
     return ATTN_OK;
 }

@@ -61,7 +61,15 @@ struct DecodeSplit {
     size_t workspace_bytes;
 };
 DecodeSplit decode_split_plan(const attn_decode_params& p, int num_sms);
-cudaError_t launch_decode(const attn_decode_params& p, const DecodeSplit& plan, cudaStream_t s);
+// Tensor maps of the tensor-core split pass: q, k, v with 64-column x 128-row boxes.
+struct DecodeMaps {
+    CUtensorMap q, k, v;
+};
+// The tensor-core split pass (attn_decode_tc.cu), then the combine kernel (attn_decode.cu).
+cudaError_t launch_decode(const attn_decode_params& p, const DecodeSplit& plan, const DecodeMaps& maps,
+                          const LaunchCommon& lc, cudaStream_t s);
+cudaError_t launch_decode_tc(const attn_decode_params& p, const DecodeSplit& plan, const DecodeMaps& maps,
+                             const LaunchCommon& lc, cudaStream_t s);
 
 // attn_fwd_sm103.cu — tcgen05 forward (bf16).
 cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);

@@ -202,7 +202,8 @@ ATTN_API attn_status_t attn_bwd_deterministic(const attn_bwd_params *p, void *st
  */
 typedef struct attn_decode_params {
     int32_t B, H;
-    int32_t nq;              /* query rows per (b, h), 1 .. 16 */
+    int32_t nq;              /* query rows per (b, h), 1 .. 128 (from 3 rows up the
+                                per-split pass runs on the tensor cores) */
     int32_t nk;              /* keys per (b, h), >= 1 */
     int32_t d;               /* 64 or 128 */
     int32_t dtype;           /* ATTN_BF16 or ATTN_F16 */

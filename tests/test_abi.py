@@ -188,7 +188,7 @@ def _decode_params(binding, **kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(nq=17), "ATTN_ERR_UNSUPPORTED"),
+    (dict(nq=129), "ATTN_ERR_UNSUPPORTED"),
     (dict(nq=-1), "ATTN_ERR_INVALID"),
     (dict(nk=0), "ATTN_ERR_INVALID"),
     (dict(d=96), "ATTN_ERR_UNSUPPORTED"),

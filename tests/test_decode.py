@@ -1,7 +1,9 @@
 """Split-KV decode (attn_decode) against the fp64 oracle's decode_forward.
 
-nq <= 16 query rows per (b, h) against nk keys; with causal the queries are
-the last nq positions. Cases cover one and several rows, key counts that are
+nq <= 128 query rows per (b, h) against nk keys; with causal the queries are
+the last nq positions. The per-split pass runs on the tensor cores with the
+query rows in a zero-padded 128-row tile. Cases cover one and several rows
+(up to 128, four softmax warps), key counts that are
 and are not multiples of the 64-key blocks, a single key, more query rows
 than keys (rows that see no key), both head dims, both 16-bit types and
 forced split counts from one range to one range per 64 keys.
@@ -55,6 +57,9 @@ def _check(A, q, k, v, causal, num_splits=0):
     (1, 1, 3, 1, 64),
     (1, 2, 16, 8, 128),   # causal: the first 8 rows see no key
     (3, 1, 2, 64, 128),
+    (1, 2, 33, 1000, 128),  # two softmax warps
+    (1, 1, 128, 300, 64),   # causal: rows beyond the keys see nothing
+    (2, 1, 100, 2500, 128),
 ])
 @pytest.mark.parametrize("causal", [False, True])
 def test_decode_matches_oracle(A, dtype, shape, causal):
@@ -95,6 +100,21 @@ def test_decode_long_cache_sampled_heads(A):
     torch.cuda.synchronize()
     assert A.attn_status() == A.ATTN_OK, A.last_error()
     for b, h in ((0, 0), (B - 1, H - 1), (3, 17)):
+        O, L = ref.decode_forward(to64(q[b:b + 1, h:h + 1]), to64(k[b:b + 1, h:h + 1]), to64(v[b:b + 1, h:h + 1]),
+                                  1 / math.sqrt(d), True)
+        assert_close_bf16(f"O[{b},{h}]", o[b:b + 1, h:h + 1], O)
+        assert_lse(lse[b:b + 1, h:h + 1], L)
+
+
+@pytest.mark.parametrize("nq", [8, 16])
+def test_decode_benchmark_shape_tensor_core_pass(A, nq):
+    # B=8 H=32 nk=8192 d=128 with 8 and 16 rows: the tensor-core split pass at full size
+    B, H, nk, d = 8, 32, 8192, 128
+    q, k, v = _case(B, H, nq, nk, d, torch.bfloat16, 730 + nq)
+    o, lse = A.attn_decode(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    for b, h in ((0, 0), (B - 1, H - 1), (5, 9)):
         O, L = ref.decode_forward(to64(q[b:b + 1, h:h + 1]), to64(k[b:b + 1, h:h + 1]), to64(v[b:b + 1, h:h + 1]),
                                   1 / math.sqrt(d), True)
         assert_close_bf16(f"O[{b},{h}]", o[b:b + 1, h:h + 1], O)
