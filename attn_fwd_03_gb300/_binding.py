@@ -205,7 +205,7 @@ def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, 
                  scale: Optional[float] = None, causal: bool = False, mask: Optional[torch.Tensor] = None,
                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                  stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """FP8 forward: q, k, v are [B, H, N, 128] E4M3 tensors (torch.float8_e4m3fn, or
+    """FP8 forward: q, k, v are [B, H, N, d] (d = 128 or 256) E4M3 tensors (torch.float8_e4m3fn, or
     uint8 holding the codes) standing for code x descale; O is bf16, LSE fp32."""
     B, H, N, d = q.shape
     if scale is None:

@@ -204,14 +204,14 @@ attn_status_t build_fwd_maps(const attn_fwd_params& p, FwdMaps* m) {
     return ATTN_OK;
 }
 
-// 4-D map of E4M3 codes over (col, row, h, b) with 128 x 128 boxes and the 128-byte swizzle.
+// 4-D map of E4M3 codes over (col, row, h, b) with 128-byte x box_rows boxes and the 128-byte swizzle.
 attn_status_t encode_u8_map(CUtensorMap* m, const char* name, const void* base, uint64_t cols, uint64_t rows,
-                            uint64_t hs, uint64_t bs, const int64_t* st) {
+                            uint64_t hs, uint64_t bs, const int64_t* st, uint32_t box_rows) {
     cuuint64_t dims[4] = {cols, rows, hs, bs};
     cuuint64_t strides[3] = {(cuuint64_t)st[2], (cuuint64_t)st[1], (cuuint64_t)st[0]};
     for (int i = 0; i < 3; ++i)
         if (strides[i] == 0) strides[i] = 16;
-    cuuint32_t box[4] = {128, 128, 1, 1};
+    cuuint32_t box[4] = {128, box_rows, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -232,7 +232,8 @@ attn_status_t check_fwd_fp8(const attn_fwd_fp8_params* p, bool* empty) {
     for (int i = 0; i < 3; ++i)
         if (!std::isfinite(ds[i]) || !(ds[i] > 0.f))
             return fail(ATTN_ERR_INVALID, "descale factors must be positive and finite");
-    if (f.d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward is built for head dim 128, got %d", f.d);
+    if (f.d != 128 && f.d != 256)
+        return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward is built for head dims 128 and 256, got %d", f.d);
     if (f.B > 65535 || f.H > 65535) return fail(ATTN_ERR_UNSUPPORTED, "B and H are limited to 65535");
     *empty = (f.B == 0 || f.H == 0 || f.N == 0);
     if (*empty) return ATTN_OK;
@@ -253,9 +254,14 @@ attn_status_t build_fp8_maps(const attn_fwd_fp8_params& p, Fp8Maps* m) {
     if (st != ATTN_OK) return st;
     const attn_fwd_params& f = p.f;
     const uint64_t N = (uint64_t)f.N, d = (uint64_t)f.d;
-    if ((st = encode_u8_map(&m->q, "q", f.q, d, N, f.H, f.B, f.q_stride)) != ATTN_OK) return st;
-    if ((st = encode_u8_map(&m->k, "k", f.k, d, N, f.H, f.B, f.k_stride)) != ATTN_OK) return st;
-    if ((st = encode_u8_map(&m->v, "v", f.v, d, N, f.H, f.B, f.v_stride)) != ATTN_OK) return st;
+    if ((st = encode_u8_map(&m->q, "q", f.q, d, N, f.H, f.B, f.q_stride, 128)) != ATTN_OK) return st;
+    if ((st = encode_u8_map(&m->k, "k", f.k, d, N, f.H, f.B, f.k_stride, 128)) != ATTN_OK) return st;
+    if ((st = encode_u8_map(&m->v, "v", f.v, d, N, f.H, f.B, f.v_stride, 128)) != ATTN_OK) return st;
+    if (f.d == 256) {
+        if ((st = encode_u8_map(&m->v64, "v", f.v, d, N, f.H, f.B, f.v_stride, 64)) != ATTN_OK) return st;
+    } else {
+        m->v64 = m->v;  // unused below head dim 256
+    }
     if (f.mask) {
         const uint64_t hm = f.mask_stride[1] != 0 ? (uint64_t)f.H : 1;
         const uint64_t bm = f.mask_stride[0] != 0 ? (uint64_t)f.B : 1;
@@ -406,7 +412,8 @@ attn_status_t attn_fwd_fp8(const attn_fwd_fp8_params* p, void* stream) {
     if ((st = device_setup(&lc)) != ATTN_OK) return st;
     Fp8Maps maps;
     if ((st = build_fp8_maps(*p, &maps)) != ATTN_OK) return st;
-    const cudaError_t e = launch_fwd_fp8(*p, maps, lc, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = p->f.d == 256 ? launch_fwd256_fp8(*p, maps, lc, static_cast<cudaStream_t>(stream))
+                                        : launch_fwd_fp8(*p, maps, lc, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_fp8 launch");
     return ATTN_OK;
 }

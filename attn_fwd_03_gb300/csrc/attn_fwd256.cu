@@ -1,4 +1,5 @@
-// attn_fwd256.cu — attention forward with head dim 256 on the sm_103a tensor cores.
+// attn_fwd256.cu — attention forward with head dim 256 on the sm_103a tensor cores,
+// for bf16, IEEE half and E4M3 (8-bit, the FP8 forward) inputs.
 //
 // The same FlashAttention-2 loop as the d = 64 / 128 forward ("What is
 // FlashAttention?", Step 3): a query tile stays on chip, key/value tiles
@@ -31,6 +32,11 @@
 // Tensor memory (512 columns x 128 lanes, lane = query row):
 //   [0,128) S (fp32)   [128,192) P (16-bit pairs)   [256,512) O (fp32)
 //
+// E4M3 inputs (kind::f8f6f4) take half the bytes: the Q tile is 32 KB, a K
+// slot holds 128 keys x 128 columns and a V slot 64 keys x 256 columns, and P
+// is rounded to E4M3 (32 TMEM columns); the Q and K descales fold into c and
+// the V descale into the epilogue, and O is bf16.
+//
 // Online softmax as in the other forward ("Explain FlashAttention and why it
 // is IO-aware", "Keep only the state needed for the final weighted average";
 // "FlashAttention", "Why it is allowed to be exact"): log2 domain with
@@ -44,26 +50,47 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "ptx_f8.cuh"
 
 namespace attn {
 namespace {
 
 using namespace ptx;
+using namespace ptx_f8;
 
 constexpr int D = 256;
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 128;  // keys per tile
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kSlotBytes = 16384;  // K: 128 rows x 64 columns; V: 32 keys x 256 columns
+constexpr int kSlotBytes = 16384;
 constexpr int kSlots = 8;
-constexpr int kQBytes = BM * D * 2;   // 64 KB, four 64-column boxes
-constexpr int kMaskBytes = BM * BN * 2;
+constexpr int kMaskBytes = BM * BN * 2;  // the additive mask is 16-bit for every input type
 constexpr int kThreads = 256;
 
-template <bool MASK>
+// Input element types: bf16, IEEE half, or E4M3 (the FP8 forward, whose O is bf16).
+enum : int { kBF16 = 0, kF16 = 1, kE4M3 = 2 };
+
+// Layout of one element type. Every shared-memory tile is made of 128-byte-swizzled rows of
+// 128 bytes, so the byte offsets of the MMA k-steps (32 bytes) are the same for both sizes.
+template <int ET>
+struct Elem {
+    static constexpr bool kF8 = ET == kE4M3;
+    static constexpr int kBytes = kF8 ? 1 : 2;
+    static constexpr int kBoxCols = 128 / kBytes;         // elements per 128-byte row: 64 or 128
+    static constexpr int kQBoxes = D / kBoxCols;          // 128-row boxes per Q tile: 4 or 2
+    static constexpr int kQBytes = BM * D * kBytes;       // 64 or 32 KB
+    static constexpr int kKSlots = D / kBoxCols;          // a K tile: one slot per box (4 or 2)
+    static constexpr int kVKeys = kSlotBytes / (D * kBytes);  // keys per V slot: 32 or 64
+    static constexpr int kVSlots = BN / kVKeys;           // 4 or 2
+    static constexpr int kStepK = 32 / kBytes;            // elements per MMA k-step: 16 or 32
+    static_assert(kKSlots == kVSlots, "K and V items take the same number of slots");
+    static constexpr int kItemSlots = kKSlots;
+};
+
+template <bool MASK, int ET>
 struct F256Cfg {
     static constexpr int kQOff = 0;
-    static constexpr int kRingOff = kQOff + kQBytes;
+    static constexpr int kRingOff = kQOff + Elem<ET>::kQBytes;
     static constexpr int kMaskOff = kRingOff + kSlots * kSlotBytes;
     static constexpr int kBarOff = kMaskOff + (MASK ? kMaskBytes : 0);
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + alignment slack
@@ -72,7 +99,8 @@ struct F256Cfg {
 struct F256Params {
     int B, H, N;
     int causal;
-    float c;  // scale * log2(e)
+    float c;          // scale * log2(e) (times the Q and K descales for E4M3)
+    float o_factor;   // the V descale for E4M3, else 1
     float* lse;
     __nv_bfloat16* o;  // 16-bit output (bf16 or half bits)
     long long o_sb, o_sh, o_sn;
@@ -137,9 +165,26 @@ __device__ __forceinline__ void kv_item(int t, int nkv, bool* is_k, int* tile) {
 
 // Descriptor of a K-major 128-row box (128-byte rows, 128-byte swizzle) at k-step kk within the box.
 __device__ __forceinline__ uint64_t kbox_desc(uint32_t box, int kk) { return sdesc_sw128(box + kk * 32, 16, 1024); }
-// Descriptor of a V slot (32 keys x four 64-column boxes of 32 rows) read MN-major at k-step kk (16 keys).
+// Descriptor of a V slot (kVKeys keys x d, as 128-byte-wide boxes of kVKeys rows) read MN-major at
+// k-step kk (kStepK keys).
+template <int ET>
 __device__ __forceinline__ uint64_t vslot_desc(uint32_t slot, int kk) {
-    return sdesc_sw128(slot + kk * (16 * 128), 32 * 128, 1024);
+    using E = Elem<ET>;
+    return sdesc_sw128(slot + kk * (E::kStepK * 128), E::kVKeys * 128, 1024);
+}
+template <int ET>
+__device__ __forceinline__ void mma_s(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    if constexpr (Elem<ET>::kF8)
+        mma_f8_ss(d, a, b, idesc, acc);
+    else
+        mma_ss(d, a, b, idesc, acc);
+}
+template <int ET>
+__device__ __forceinline__ void mma_t(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    if constexpr (Elem<ET>::kF8)
+        mma_f8_ts(d, a, b, idesc, acc);
+    else
+        mma_ts(d, a, b, idesc, acc);
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -149,14 +194,16 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
         if (globaltimer() - t0 > timeout_ns) break;
 }
 
-template <bool MASK, bool F16>
+template <bool MASK, int ET>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v32, const __grid_constant__ CUtensorMap tm_mask,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_mask,
                   const F256Params p) {
-    using Cfg = F256Cfg<MASK>;
-    constexpr uint32_t kIdescS = idesc_h16(BM, BN, false, false, F16);
-    constexpr uint32_t kIdescO = idesc_h16(BM, D, false, true, F16);
+    using Cfg = F256Cfg<MASK, ET>;
+    using E = Elem<ET>;
+    constexpr bool F16 = ET == kF16;  // 16-bit storage of the mask (and of O) is half, else bf16
+    constexpr uint32_t kIdescS = E::kF8 ? idesc_e4m3(BM, BN, false, false) : idesc_h16(BM, BN, false, false, F16);
+    constexpr uint32_t kIdescO = E::kF8 ? idesc_e4m3(BM, D, false, true) : idesc_h16(BM, D, false, true, F16);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     F256Barriers& bar = *reinterpret_cast<F256Barriers*>(smem + Cfg::kBarOff);
@@ -197,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v32);
+            prefetch_tmap(&tm_v);
         }
         __syncwarp();
         uint32_t n = 0, n_units = 0;  // slots filled so far, units started
@@ -207,28 +254,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = mbar_wait_warp(&bar.q_empty, (n_units & 1) ^ 1, wc);
             if (!ok) break;
             if (elect_one()) {
-                mbar_arrive_expect_tx(&bar.q_full, kQBytes);
-                for (int bx = 0; bx < 4; ++bx)
-                    tma_load_4d(smem + Cfg::kQOff + bx * BM * 128, &tm_q, &bar.q_full, bx * 64, w.qt * BM, w.h, w.b);
+                mbar_arrive_expect_tx(&bar.q_full, E::kQBytes);
+                for (int bx = 0; bx < E::kQBoxes; ++bx)
+                    tma_load_4d(smem + Cfg::kQOff + bx * BM * 128, &tm_q, &bar.q_full, bx * E::kBoxCols, w.qt * BM,
+                                w.h, w.b);
             }
             __syncwarp();
             for (int t = 0; t < 2 * w.nkv && ok; ++t) {
                 bool is_k;
                 int j;
                 kv_item(t, w.nkv, &is_k, &j);
-                for (int q4 = 0; q4 < 4; ++q4, ++n) {
+                for (int q4 = 0; q4 < E::kItemSlots; ++q4, ++n) {
                     const uint32_t s = n % kSlots;
                     ok = mbar_wait_warp(&bar.slot_empty[s], ((n / kSlots) & 1) ^ 1, wc);
                     if (!ok) break;
                     if (elect_one()) {
                         mbar_arrive_expect_tx(&bar.slot_full[s], kSlotBytes);
                         uint8_t* dst = smem + Cfg::kRingOff + s * kSlotBytes;
-                        if (is_k) {  // columns [64 q4, 64 q4 + 64) of K_j
-                            tma_load_4d(dst, &tm_k, &bar.slot_full[s], q4 * 64, j * BN, w.h, w.b);
-                        } else {  // keys [32 q4, 32 q4 + 32) of V_j, as four 64-column boxes
-                            for (int bx = 0; bx < 4; ++bx)
-                                tma_load_4d(dst + bx * 32 * 128, &tm_v32, &bar.slot_full[s], bx * 64,
-                                            j * BN + q4 * 32, w.h, w.b);
+                        if (is_k) {  // box q4 (128-byte-wide columns) of K_j
+                            tma_load_4d(dst, &tm_k, &bar.slot_full[s], q4 * E::kBoxCols, j * BN, w.h, w.b);
+                        } else {  // keys [kVKeys q4, kVKeys (q4 + 1)) of V_j, as 128-byte-wide boxes
+                            for (int bx = 0; bx < E::kQBoxes; ++bx)
+                                tma_load_4d(dst + bx * E::kVKeys * 128, &tm_v, &bar.slot_full[s], bx * E::kBoxCols,
+                                            j * BN + q4 * E::kVKeys, w.h, w.b);
                         }
                     }
                     __syncwarp();
@@ -281,18 +329,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = mbar_wait_warp(&bar.s_free, (n_s - 1) & 1, wc);
                         if (!ok) break;
                     }
-                    for (int bx = 0; bx < 4 && ok; ++bx, ++n) {
+                    for (int bx = 0; bx < E::kItemSlots && ok; ++bx, ++n) {
                         const uint32_t s = n % kSlots;
                         ok = mbar_wait_warp(&bar.slot_full[s], (n / kSlots) & 1, wc);
                         if (!ok) break;
                         tc_fence_after();
                         if (elect_one()) {
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tS, kbox_desc(sQ + bx * BM * 128, kk), kbox_desc(sRing + s * kSlotBytes, kk),
-                                       kIdescS, (bx > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk)  // four 32-byte k-steps per 128-byte row
+                                mma_s<ET>(tS, kbox_desc(sQ + bx * BM * 128, kk), kbox_desc(sRing + s * kSlotBytes, kk),
+                                          kIdescS, (bx > 0 || kk > 0) ? 1u : 0u);
                             mma_commit(&bar.slot_empty[s]);
-                            if (bx == 3) {
+                            if (bx == E::kItemSlots - 1) {
                                 mma_commit(&bar.s_full);
                                 if (j == w.nkv - 1) mma_commit(&bar.q_empty);  // last read of Q
                             }
@@ -309,18 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait_warp(&bar.p_full, n_p & 1, wc);
                     if (!ok) break;
                     ++n_p;
-                    for (int q4 = 0; q4 < 4 && ok; ++q4, ++n) {
+                    for (int q4 = 0; q4 < E::kItemSlots && ok; ++q4, ++n) {
                         const uint32_t s = n % kSlots;
                         ok = mbar_wait_warp(&bar.slot_full[s], (n / kSlots) & 1, wc);
                         if (!ok) break;
                         tc_fence_after();
                         if (elect_one()) {
+                            // kVKeys keys per slot in k-steps of kStepK; P holds 8 TMEM columns per k-step
 #pragma unroll
-                            for (int kk = 0; kk < 2; ++kk)
-                                mma_ts(tO, tP + (2 * q4 + kk) * 8, vslot_desc(sRing + s * kSlotBytes, kk), kIdescO,
-                                       (j > 0 || q4 > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < E::kVKeys / E::kStepK; ++kk)
+                                mma_t<ET>(tO, tP + (2 * q4 + kk) * 8, vslot_desc<ET>(sRing + s * kSlotBytes, kk),
+                                          kIdescO, (j > 0 || q4 > 0 || kk > 0) ? 1u : 0u);
                             mma_commit(&bar.slot_empty[s]);
-                            if (q4 == 3) mma_commit(&bar.pv_done);
+                            if (q4 == E::kItemSlots - 1) mma_commit(&bar.pv_done);
                         }
                         __syncwarp();
                     }
@@ -418,16 +467,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
                 const float2 cc2 = make_float2(cc, cc), nm2 = make_float2(neg_m, neg_m);
                 float2 suma = make_float2(0.f, 0.f), sumb = make_float2(0.f, 0.f);
+                if constexpr (E::kF8) {
+                    // P as E4M3 quads packed into su[0..31] (quad i from columns 4i..4i+3, already read)
 #pragma unroll
-                for (int i = 0; i < BN / 2; ++i) {
-                    const float2 x =
-                        ffma2(make_float2(__uint_as_float(su[2 * i]), __uint_as_float(su[2 * i + 1])), cc2, nm2);
-                    const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-                    if (i & 1)
-                        sumb = fadd2(sumb, pp);
-                    else
-                        suma = fadd2(suma, pp);
-                    su[i] = pack_h16<F16>(pp.x, pp.y);
+                    for (int i = 0; i < BN / 4; ++i) {
+                        const float2 xa = ffma2(
+                            make_float2(__uint_as_float(su[4 * i]), __uint_as_float(su[4 * i + 1])), cc2, nm2);
+                        const float2 xb = ffma2(
+                            make_float2(__uint_as_float(su[4 * i + 2]), __uint_as_float(su[4 * i + 3])), cc2, nm2);
+                        const float2 pa = make_float2(ex2(xa.x), ex2(xa.y));
+                        const float2 pb = make_float2(ex2(xb.x), ex2(xb.y));
+                        suma = fadd2(suma, pa);
+                        sumb = fadd2(sumb, pb);
+                        su[i] = pack_e4m3x4(pa.x, pa.y, pb.x, pb.y);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < BN / 2; ++i) {
+                        const float2 x =
+                            ffma2(make_float2(__uint_as_float(su[2 * i]), __uint_as_float(su[2 * i + 1])), cc2, nm2);
+                        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+                        if (i & 1)
+                            sumb = fadd2(sumb, pp);
+                        else
+                            suma = fadd2(suma, pp);
+                        su[i] = pack_h16<F16>(pp.x, pp.y);
+                    }
                 }
                 if (j > 0) {  // the product of key tile j-1 has read P and written O
                     ok = mbar_wait(&bar.pv_done, pvcnt & 1, wc);
@@ -454,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 tmem_st32_at<0>(tP + 0, su);
-                tmem_st32_at<32>(tP + 32, su);
+                if constexpr (!E::kF8) tmem_st32_at<32>(tP + 32, su);
                 l = l * alpha + ((suma.x + suma.y) + (sumb.x + sumb.y));
                 tmem_wait_st();
                 tc_fence_before();
@@ -467,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ++pvcnt;
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.o_factor / l : 0.f;
             __nv_bfloat16* orow = p.o + w.b * p.o_sb + w.h * p.o_sh + (long long)row * p.o_sn;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -500,19 +565,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
-template <bool MASK, bool F16>
-cudaError_t launch256(const attn_fwd_params& prm, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s) {
-    using Cfg = F256Cfg<MASK>;
+template <bool MASK, int ET>
+cudaError_t launch256(const attn_fwd_params& prm, float c, float o_factor, const CUtensorMap& tm_q,
+                      const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_mask,
+                      const LaunchCommon& lc, cudaStream_t s) {
+    using Cfg = F256Cfg<MASK, ET>;
     static_assert(Cfg::kSmemBytes <= 232448, "shared memory budget");
     cudaError_t e =
-        cudaFuncSetAttribute(fwd256_kernel<MASK, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        cudaFuncSetAttribute(fwd256_kernel<MASK, ET>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
     if (e != cudaSuccess) return e;
     F256Params p{};
     p.B = prm.B;
     p.H = prm.H;
     p.N = prm.N;
     p.causal = prm.causal;
-    p.c = prm.scale * kLog2e;
+    p.c = c;
+    p.o_factor = o_factor;
     p.lse = prm.lse;
     p.o = static_cast<__nv_bfloat16*>(prm.o);
     p.o_sb = prm.o_stride[0];
@@ -526,16 +594,27 @@ cudaError_t launch256(const attn_fwd_params& prm, const FwdMaps& maps, const Lau
     p.err = lc.err;
     p.timeout_ns = lc.timeout_ns;
     const int grid = p.num_units < lc.num_sms ? p.num_units : lc.num_sms;
-    fwd256_kernel<MASK, F16><<<grid, kThreads, Cfg::kSmemBytes, s>>>(maps.q, maps.k, maps.v32, maps.mask, p);
+    fwd256_kernel<MASK, ET><<<grid, kThreads, Cfg::kSmemBytes, s>>>(tm_q, tm_k, tm_v, tm_mask, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd256(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s) {
+    const float c = p.scale * kLog2e;
     const bool mask = p.mask != nullptr, f16 = p.dtype == ATTN_F16;
-    if (mask) return f16 ? launch256<true, true>(p, maps, lc, s) : launch256<true, false>(p, maps, lc, s);
-    return f16 ? launch256<false, true>(p, maps, lc, s) : launch256<false, false>(p, maps, lc, s);
+    if (mask)
+        return f16 ? launch256<true, kF16>(p, c, 1.f, maps.q, maps.k, maps.v32, maps.mask, lc, s)
+                   : launch256<true, kBF16>(p, c, 1.f, maps.q, maps.k, maps.v32, maps.mask, lc, s);
+    return f16 ? launch256<false, kF16>(p, c, 1.f, maps.q, maps.k, maps.v32, maps.mask, lc, s)
+               : launch256<false, kBF16>(p, c, 1.f, maps.q, maps.k, maps.v32, maps.mask, lc, s);
+}
+
+cudaError_t launch_fwd256_fp8(const attn_fwd_fp8_params& p, const Fp8Maps& maps, const LaunchCommon& lc,
+                              cudaStream_t s) {
+    const float c = p.f.scale * kLog2e * p.q_descale * p.k_descale;
+    if (p.f.mask) return launch256<true, kE4M3>(p.f, c, p.v_descale, maps.q, maps.k, maps.v64, maps.mask, lc, s);
+    return launch256<false, kE4M3>(p.f, c, p.v_descale, maps.q, maps.k, maps.v64, maps.mask, lc, s);
 }
 
 }  // namespace attn

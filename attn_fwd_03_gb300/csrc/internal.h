@@ -74,13 +74,17 @@ cudaError_t launch_decode_tc(const attn_decode_params& p, const DecodeSplit& pla
 // attn_fwd_sm103.cu — tcgen05 forward (bf16).
 cudaError_t launch_fwd_tc(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);
 
-// Tensor maps for the FP8 forward: E4M3 q, k, v (128 x 128-byte boxes), bf16 mask.
+// Tensor maps for the FP8 forward: E4M3 q, k, v (128-byte x 128-row boxes), bf16 mask, and
+// for head dim 256 V again with 64-row boxes.
 struct Fp8Maps {
-    CUtensorMap q, k, v, mask;
+    CUtensorMap q, k, v, mask, v64;
 };
 // attn_fwd_fp8.cu — tcgen05 kind::f8f6f4 forward, head dim 128.
 cudaError_t launch_fwd_fp8(const attn_fwd_fp8_params& p, const Fp8Maps& maps, const LaunchCommon& lc,
                            cudaStream_t s);
+// attn_fwd256.cu — the same for head dim 256.
+cudaError_t launch_fwd256_fp8(const attn_fwd_fp8_params& p, const Fp8Maps& maps, const LaunchCommon& lc,
+                              cudaStream_t s);
 
 // attn_fwd256.cu — tcgen05 forward for head dim 256 (bf16 / fp16).
 cudaError_t launch_fwd256(const attn_fwd_params& p, const FwdMaps& maps, const LaunchCommon& lc, cudaStream_t s);

@@ -127,7 +127,7 @@ ATTN_API attn_status_t attn_fwd(const attn_fwd_params *p, void *stream);
  * stand for code value x descale. The result is the attention of those
  * values, as attn_fwd defines it, with the products on the 8-bit tensor
  * cores and P rounded to E4M3 before it multiplies V.
- *  - f.dtype = ATTN_E4M3; f.d = 128. q, k, v strides count bytes (elements)
+ *  - f.dtype = ATTN_E4M3; f.d = 128 or 256. q, k, v strides count bytes (elements)
  *    and must be multiples of 16. f.o is bf16 [B, H, N, d] (strides in bf16
  *    elements); f.mask, when given, is bf16 as for attn_fwd; f.lse as attn_fwd.
  *  - Accuracy: each probability carries up to 2^-4 relative rounding, so O

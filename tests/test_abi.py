@@ -228,6 +228,7 @@ def _fp8_params(binding, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(d=64), "ATTN_ERR_UNSUPPORTED"),
+    (dict(d=192), "ATTN_ERR_UNSUPPORTED"),
     (dict(dtype=0), "ATTN_ERR_UNSUPPORTED"),  # a 16-bit dtype goes through attn_fwd
     (dict(descale=(0.5, 0.0, 0.5)), "ATTN_ERR_INVALID"),
     (dict(descale=(0.5, 0.5, float("inf"))), "ATTN_ERR_INVALID"),

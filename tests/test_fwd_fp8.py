@@ -1,4 +1,5 @@
-"""The FP8 (E4M3) forward against the fp64 oracle of the values the codes stand for.
+"""The FP8 (E4M3) forward (head dims 128 and 256) against the fp64 oracle of the
+values the codes stand for.
 
 Tolerance, derived from the kernel's arithmetic (written out here, not fitted):
 the scores are exact products of E4M3 values summed in fp32, and the softmax
@@ -87,30 +88,34 @@ def _run(A, inp, causal, scale, mask=None):
     return o, lse
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 255, 257, 600])
 @pytest.mark.parametrize("causal", [False, True])
-def test_edge_lengths(A, N, causal):
-    inp = _inputs((1, 2, N, 128), 4000 + N)
-    o, lse = _run(A, inp, causal, 1 / math.sqrt(128))
-    _check(o, lse, _bound_and_ref(inp, 1 / math.sqrt(128), causal, None))
+def test_edge_lengths(A, d, N, causal):
+    inp = _inputs((1, 2, N, d), 4000 + N + d)
+    o, lse = _run(A, inp, causal, 1 / math.sqrt(d))
+    _check(o, lse, _bound_and_ref(inp, 1 / math.sqrt(d), causal, None))
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_several_units_per_cta(A, causal):
-    inp = _inputs((2, 12, 700, 128), 4100)
-    o, lse = _run(A, inp, causal, 1 / math.sqrt(128))
-    _check(o, lse, _bound_and_ref(inp, 1 / math.sqrt(128), causal, None, heads=[(0, 0), (1, 11), (0, 5)]))
+def test_several_units_per_cta(A, d, causal):
+    inp = _inputs((2, 12, 700, d), 4100)
+    o, lse = _run(A, inp, causal, 1 / math.sqrt(d))
+    _check(o, lse, _bound_and_ref(inp, 1 / math.sqrt(d), causal, None, heads=[(0, 0), (1, 11), (0, 5)]))
 
 
-def test_large_scores_rescale(A):
-    inp = _inputs((1, 2, 500, 128), 4200, mult=math.sqrt(30.0))
-    o, lse = _run(A, inp, True, 1 / math.sqrt(128))
-    _check(o, lse, _bound_and_ref(inp, 1 / math.sqrt(128), True, None))
+@pytest.mark.parametrize("d", [128, 256])
+def test_large_scores_rescale(A, d):
+    inp = _inputs((1, 2, 500, d), 4200, mult=math.sqrt(30.0))
+    o, lse = _run(A, inp, True, 1 / math.sqrt(d))
+    _check(o, lse, _bound_and_ref(inp, 1 / math.sqrt(d), True, None))
 
 
-def test_additive_mask_with_masked_rows(A):
+@pytest.mark.parametrize("d", [128, 256])
+def test_additive_mask_with_masked_rows(A, d):
     B, H, N = 2, 2, 264
-    inp = _inputs((B, H, N, 128), 4300)
+    inp = _inputs((B, H, N, d), 4300)
     g = torch.Generator().manual_seed(43)
     mask = torch.randn(B, 1, N, N, generator=g) * 2
     mask[torch.rand(mask.shape, generator=g) < 0.2] = float("-inf")

@@ -154,6 +154,7 @@ def make_inputs(w: Workload, with_grad: Optional[bool] = None, shape=None) -> Di
 FP8_WORKLOADS: Dict[int, Workload] = {
     9: Workload(9, "b1_h32_n8192_d128_e4m3_fwd", 1, 32, 8192, 128, "e4m3", False, False, False),
     10: Workload(10, "b1_h16_n32768_d128_e4m3_causal_fwd", 1, 16, 32768, 128, "e4m3", True, False, False),
+    11: Workload(11, "b1_h16_n8192_d256_e4m3_fwd", 1, 16, 8192, 256, "e4m3", False, False, False),
 }
 
 
