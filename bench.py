@@ -576,6 +576,9 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-all", action="store_true", help="skip the per-workload forward/backward table")
+    ap.add_argument("--decode", type=int, default=None, metavar="NQ",
+                    help="time only the split-KV decode entry of the table with NQ query rows "
+                         "(B=8 H=32 nk=8192 d=128) and print it as one JSON line")
     ap.add_argument("--table-workload", default=None,
                     help="time only this entry of the per-workload table (a workload name from workloads.py, "
                          "e.g. under a profiler) and print it as one JSON line")
@@ -587,6 +590,14 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.table_workload is not None:
         run_table_entry(args)
+        return
+    if args.decode is not None:
+        import torch
+        import attn_fwd_03_gb300 as A
+        peaks, _ = load_peaks()
+        r = measure_decode(A, torch.device("cuda", 0), peaks["hbm_gbs"], args.decode, steps=args.steps,
+                           warmup=args.warmup)
+        print(json.dumps({"workload": f"decode_b8_h32_nq{args.decode}_nk8192_d128_bf16_causal", **r}), flush=True)
         return
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":
