@@ -186,6 +186,9 @@ __global__ void __launch_bounds__(384, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // No global memory is touched above: from here on the pre-pass must be complete.
+    grid_dep_launch();
+    grid_dep_wait();
     const uint32_t tmem = bar.tmem_base;
     const uint32_t sK = smem_u32(smem + Cfg::kKOff), sV = smem_u32(smem + Cfg::kVOff);
     const uint32_t sDS = smem_u32(smem + Cfg::kDSOff);
@@ -636,6 +639,9 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // No global memory is touched above: from here on the pre-pass must be complete.
+    grid_dep_launch();
+    grid_dep_wait();
     const uint32_t tmem = bar.tmem_base;
 
     if (warp == 8) {
@@ -1087,9 +1093,9 @@ cudaError_t launch_bwd_tc_t(const attn_bwd_params& prm, const BwdMaps& maps, con
     // d = 64: persistent, one CTA per SM walking the units; d = 128: one CTA per unit
     const unsigned grid = D == 64 ? (unsigned)(p.num_units < lc.num_sms ? p.num_units : lc.num_sms)
                                   : (unsigned)p.num_units;
-    kernel<<<grid, D == 64 ? 512 : 384, kSmem, s>>>(maps.q, maps.k, maps.v, maps.dout, maps.mask, maps.dq_acc,
-                                                     maps.dk, maps.dv, p);
-    return cudaGetLastError();
+    e = launch_pdl(kernel, dim3(grid), dim3(D == 64 ? 512 : 384), kSmem, s, maps.q, maps.k, maps.v, maps.dout,
+                   maps.mask, maps.dq_acc, maps.dk, maps.dv, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 

@@ -229,6 +229,9 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // No global memory is touched above: from here on the previous kernel must be complete.
+    grid_dep_launch();
+    grid_dep_wait();
     const uint32_t tmem = bar.tmem_base;
     const uint32_t sQ = smem_u32(smem + Cfg::kQOff);
     const uint32_t sKV = smem_u32(smem + Cfg::kKVOff);
@@ -711,8 +714,9 @@ cudaError_t launch_tc(const attn_fwd_params& prm, const FwdMaps& maps, const Lau
     p.timeout_ns = lc.timeout_ns;
     p.stall_after = lc.stall_after;
     const int grid = p.num_units < lc.num_sms ? p.num_units : lc.num_sms;
-    fwd_tc_kernel<D, MASK, F16><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(maps.q, maps.k, maps.v, maps.mask, p);
-    return cudaGetLastError();
+    e = launch_pdl(fwd_tc_kernel<D, MASK, F16>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, s,
+                   maps.q, maps.k, maps.v, maps.mask, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 

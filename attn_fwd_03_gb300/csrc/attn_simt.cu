@@ -175,6 +175,8 @@ constexpr int kRowsPerThread = 4;
 
 template <int D, typename IDX, bool F16>
 __global__ void __launch_bounds__(256) bwd_prepass_kernel(SimtArgs a, float* stats, float* dq_acc, int* err) {
+    ptx::grid_dep_wait();    // O and LSE may come from the forward just before
+    ptx::grid_dep_launch();  // the main kernel may start its prologue
     constexpr int G = D / 8;            // threads per row
     constexpr int RPB = 256 / G;        // rows per block and step
     const IDX n_pad = (IDX)((a.N + 127) / 128 * 128);
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(256) bwd_prepass_kernel(SimtArgs a, float* sta
 // ------------------------------------------------------------ dQ finalize
 template <int D, typename IDX, bool F16>
 __global__ void __launch_bounds__(256) bwd_dq_finalize_kernel(SimtArgs a, const float* dq_acc, int* err) {
+    ptx::grid_dep_wait();  // every reduction into the accumulator has landed
     constexpr int G = D / 8;
     constexpr int RPB = 256 / G;
     const IDX rows = (IDX)a.B * (IDX)a.H * (IDX)a.N;
@@ -335,18 +338,20 @@ RowGrid row_grid(long long rows, int d) {
     return RowGrid{(unsigned)blocks, rows + blocks * rpb < (1ll << 31)};
 }
 template <int D, bool F16>
-void prepass_t(const RowGrid& g, const SimtArgs& a, const BwdWorkspace& ws, int* err, cudaStream_t s) {
+cudaError_t prepass_t(const RowGrid& g, const SimtArgs& a, const BwdWorkspace& ws, int* err, cudaStream_t s) {
     if (g.idx32)
-        bwd_prepass_kernel<D, unsigned, F16><<<g.blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
-    else
-        bwd_prepass_kernel<D, unsigned long long, F16><<<g.blocks, 256, 0, s>>>(a, ws.stats, ws.dq_acc, err);
+        return launch_pdl(bwd_prepass_kernel<D, unsigned, F16>, dim3(g.blocks), dim3(256), 0, s, a, ws.stats,
+                          ws.dq_acc, err);
+    return launch_pdl(bwd_prepass_kernel<D, unsigned long long, F16>, dim3(g.blocks), dim3(256), 0, s, a, ws.stats,
+                      ws.dq_acc, err);
 }
 template <int D, bool F16>
-void finalize_t(const RowGrid& g, const SimtArgs& a, const BwdWorkspace& ws, int* err, cudaStream_t s) {
+cudaError_t finalize_t(const RowGrid& g, const SimtArgs& a, const BwdWorkspace& ws, int* err, cudaStream_t s) {
+    const float* acc = ws.dq_acc;
     if (g.idx32)
-        bwd_dq_finalize_kernel<D, unsigned, F16><<<g.blocks, 256, 0, s>>>(a, ws.dq_acc, err);
-    else
-        bwd_dq_finalize_kernel<D, unsigned long long, F16><<<g.blocks, 256, 0, s>>>(a, ws.dq_acc, err);
+        return launch_pdl(bwd_dq_finalize_kernel<D, unsigned, F16>, dim3(g.blocks), dim3(256), 0, s, a, acc, err);
+    return launch_pdl(bwd_dq_finalize_kernel<D, unsigned long long, F16>, dim3(g.blocks), dim3(256), 0, s, a, acc,
+                      err);
 }
 }  // namespace
 
@@ -354,22 +359,20 @@ cudaError_t launch_bwd_prepass(const attn_bwd_params& p, const BwdWorkspace& ws,
     const SimtArgs a = make_bwd_args(p, ws);
     const RowGrid g = row_grid((long long)p.fwd.B * p.fwd.H * ((p.fwd.N + 127) / 128 * 128), p.fwd.d);
     const bool f16 = p.fwd.dtype == ATTN_F16;
-    if (p.fwd.d == 64)
-        f16 ? prepass_t<64, true>(g, a, ws, err, s) : prepass_t<64, false>(g, a, ws, err, s);
-    else
-        f16 ? prepass_t<128, true>(g, a, ws, err, s) : prepass_t<128, false>(g, a, ws, err, s);
-    return cudaGetLastError();
+    const cudaError_t e = p.fwd.d == 64
+                              ? (f16 ? prepass_t<64, true>(g, a, ws, err, s) : prepass_t<64, false>(g, a, ws, err, s))
+                              : (f16 ? prepass_t<128, true>(g, a, ws, err, s) : prepass_t<128, false>(g, a, ws, err, s));
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_finalize(const attn_bwd_params& p, const BwdWorkspace& ws, int* err, cudaStream_t s) {
     const SimtArgs a = make_bwd_args(p, ws);
     const RowGrid g = row_grid((long long)p.fwd.B * p.fwd.H * p.fwd.N, p.fwd.d);
     const bool f16 = p.fwd.dtype == ATTN_F16;
-    if (p.fwd.d == 64)
-        f16 ? finalize_t<64, true>(g, a, ws, err, s) : finalize_t<64, false>(g, a, ws, err, s);
-    else
-        f16 ? finalize_t<128, true>(g, a, ws, err, s) : finalize_t<128, false>(g, a, ws, err, s);
-    return cudaGetLastError();
+    const cudaError_t e =
+        p.fwd.d == 64 ? (f16 ? finalize_t<64, true>(g, a, ws, err, s) : finalize_t<64, false>(g, a, ws, err, s))
+                      : (f16 ? finalize_t<128, true>(g, a, ws, err, s) : finalize_t<128, false>(g, a, ws, err, s));
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace attn

@@ -21,6 +21,27 @@ struct LaunchCommon {
     int num_sms;          // SM count of the current device
 };
 
+// Launches `kernel` with programmatic stream serialization, so that it may start while the
+// kernel before it in the stream still runs. Every kernel launched this way executes
+// griddepcontrol.wait before its first global memory access, which returns once the previous
+// kernel has completed and its writes are visible; a kernel that follows a non-kernel
+// operation is serialised as usual.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       const Args&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Tensor maps for the tcgen05 forward (built by the host API).
 struct FwdMaps {
     CUtensorMap q, k, v, o, mask;

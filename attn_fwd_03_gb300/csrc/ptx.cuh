@@ -349,6 +349,13 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
     return d;
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization
+// may start while the kernel before it in the stream is still running: griddepcontrol.wait
+// returns once that kernel has completed and its memory operations are visible (at once
+// when there is none), and launch_dependents lets the next kernel start its own prologue.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
