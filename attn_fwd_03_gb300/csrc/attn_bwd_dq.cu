@@ -197,6 +197,9 @@ __global__ void __launch_bounds__(DqCfg<D, MASK>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // No global memory is touched above: from here on the previous kernel must be complete.
+    grid_dep_launch();
+    grid_dep_wait();
     const uint32_t tmem = bar.tmem_base;
     const uint32_t sQ = smem_u32(smem + Cfg::kQOff);
     const uint32_t sDO = sQ + Cfg::kTileBytes;
@@ -505,9 +508,9 @@ cudaError_t launch_dq(const attn_bwd_params& prm, const BwdMaps& maps, const Bwd
     p.err = lc.err;
     p.timeout_ns = lc.timeout_ns;
     const int grid = p.num_units < lc.num_sms ? p.num_units : lc.num_sms;
-    bwd_dq_kernel<D, MASK, F16>
-        <<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(maps.q, maps.k, maps.v, maps.dout, maps.mask, p);
-    return cudaGetLastError();
+    e = launch_pdl(bwd_dq_kernel<D, MASK, F16>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, s, maps.q, maps.k,
+                   maps.v, maps.dout, maps.mask, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <bool F16>

@@ -45,6 +45,7 @@ constexpr int rec_floats() {
 
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) decode_combine_kernel(CombineArgs a) {
+    ptx::grid_dep_wait();  // the split pass's records have landed
     constexpr int PER = D / 32;  // output columns per lane
     const int warp_g = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int rows = a.B * a.H * a.nq;
@@ -83,8 +84,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(CombineArgs a) {
 template <int D, bool F16>
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
     const int rows = a.B * a.H * a.nq;
-    decode_combine_kernel<D, F16><<<(rows + 7) / 8, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    const cudaError_t e = launch_pdl(decode_combine_kernel<D, F16>, dim3((rows + 7) / 8), dim3(256), 0, s, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

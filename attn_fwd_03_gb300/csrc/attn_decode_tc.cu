@@ -163,6 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // No global memory is touched above: from here on the previous kernel must be complete.
+    grid_dep_launch();
+    grid_dep_wait();
     const uint32_t tmem = bar.tmem_base;
     const uint32_t sQ = smem_u32(smem + Cfg::kQOff);
     const uint32_t sRing = smem_u32(smem + Cfg::kRingOff);
@@ -419,15 +422,15 @@ cudaError_t launch_decode_tc(const attn_decode_params& prm, const DecodeSplit& p
         if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DtcCfg<64>::kSmemBytes)) !=
             cudaSuccess)
             return e;
-        k<<<grid, kThreads, DtcCfg<64>::kSmemBytes, s>>>(maps.q, maps.k, maps.v, p);
+        e = launch_pdl(k, dim3(grid), dim3(kThreads), DtcCfg<64>::kSmemBytes, s, maps.q, maps.k, maps.v, p);
     } else {
         auto k = f16 ? decode_tc_kernel<128, true> : decode_tc_kernel<128, false>;
         if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DtcCfg<128>::kSmemBytes)) !=
             cudaSuccess)
             return e;
-        k<<<grid, kThreads, DtcCfg<128>::kSmemBytes, s>>>(maps.q, maps.k, maps.v, p);
+        e = launch_pdl(k, dim3(grid), dim3(kThreads), DtcCfg<128>::kSmemBytes, s, maps.q, maps.k, maps.v, p);
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace attn

@@ -235,6 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // No global memory is touched above: from here on the previous kernel must be complete.
+    grid_dep_launch();
+    grid_dep_wait();
     const uint32_t tmem = bar.tmem_base;
     const uint32_t sQ = smem_u32(smem + Cfg::kQOff);
     const uint32_t sRing = smem_u32(smem + Cfg::kRingOff);
@@ -594,8 +597,9 @@ cudaError_t launch256(const attn_fwd_params& prm, float c, float o_factor, const
     p.err = lc.err;
     p.timeout_ns = lc.timeout_ns;
     const int grid = p.num_units < lc.num_sms ? p.num_units : lc.num_sms;
-    fwd256_kernel<MASK, ET><<<grid, kThreads, Cfg::kSmemBytes, s>>>(tm_q, tm_k, tm_v, tm_mask, p);
-    return cudaGetLastError();
+    e = launch_pdl(fwd256_kernel<MASK, ET>, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, s, tm_q, tm_k, tm_v, tm_mask,
+                   p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

@@ -188,6 +188,9 @@ __global__ void __launch_bounds__(F8Cfg<MASK>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // No global memory is touched above: from here on the previous kernel must be complete.
+    grid_dep_launch();
+    grid_dep_wait();
     const uint32_t tmem = bar.tmem_base;
     const uint32_t sQ = smem_u32(smem + Cfg::kQOff);
     const uint32_t sKV = smem_u32(smem + Cfg::kKVOff);
@@ -527,8 +530,9 @@ cudaError_t launch_f8(const attn_fwd_fp8_params& prm, const Fp8Maps& maps, const
     p.err = lc.err;
     p.timeout_ns = lc.timeout_ns;
     const int grid = p.num_units < lc.num_sms ? p.num_units : lc.num_sms;
-    fwd_fp8_kernel<MASK><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(maps.q, maps.k, maps.v, maps.mask, p);
-    return cudaGetLastError();
+    e = launch_pdl(fwd_fp8_kernel<MASK>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, s, maps.q, maps.k, maps.v,
+                   maps.mask, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
