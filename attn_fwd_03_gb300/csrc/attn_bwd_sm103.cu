@@ -782,6 +782,9 @@ __global__ void __launch_bounds__(512, 1)
                         mma_commit(&bar.buf_free[gu % 3]);
                         // the tile's last reads of Q and dO (its scores completed before ds_ready)
                         if (hv == 1) mma_commit(&bar.st_empty[sv]);
+                        // dV and dK of this unit are complete: the drain reads them out before the
+                        // unit's last dQ, so the next unit's gradients need not wait for that dQ
+                        if (vl == n_half - 1) mma_commit(&bar.kv_done);
                     }
                     __syncwarp();
                     if (hv == 1) {
@@ -803,10 +806,7 @@ __global__ void __launch_bounds__(512, 1)
                         __syncwarp();
                     }
                 }
-                if (elect_one() && ok) {
-                    mma_commit(&bar.kv_done);  // dV and dK of this unit are complete
-                    mma_commit(&bar.kv_free[n & 1]);  // and its dQ products have read K
-                }
+                if (elect_one() && ok) mma_commit(&bar.kv_free[n & 1]);  // its dQ products have read K
                 __syncwarp();
             }
         }
@@ -932,7 +932,7 @@ __global__ void __launch_bounds__(512, 1)
 
     else if (warp >= 12) {
         // ------------------------------------------------ dQ drain (thread = query row of the tile),
-        // then each unit's dV / dK epilogue
+        // and each unit's dV / dK epilogue
         // scale * dQ goes to shared memory in the 128-byte-swizzled layout of the
         // accumulator's tensor map (box bx = columns 32 bx .. 32 bx + 31), and one
         // thread adds both boxes into the fp32 accumulator with TMA reductions.
@@ -947,6 +947,64 @@ __global__ void __launch_bounds__(512, 1)
         for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku), ++n) {
             const Unit64 w = unit64(p, u);
             for (int it = 0; it < w.n_it && ok; ++it, ++gt) {
+                if (it == w.n_it - 1) {
+                    // unit epilogue (thread = key row), taken before the unit's last dQ: dV and
+                    // dK are complete once their last products are (kv_done), and reading them
+                    // out here lets the next unit's gradients start while that dQ is still in
+                    // the tensor core. They leave through shared memory and TMA stores, so the
+                    // P^T / dS^T warps go straight on to the next unit. The staging area is the
+                    // dS buffer of the unit's second-to-last tile, which its dQ product has
+                    // read; the next tile to write that buffer is the next unit's first, after
+                    // these stores have read it (epi_free). Rows beyond N are clipped by the maps.
+                    const int gl = gt;  // this unit's last tile
+                    ok = mbar_wait(&bar.kv_done, n & 1, wc);
+                    if (gl >= 1) ok = ok && mbar_wait(&bar.dq_done[(gl - 1) & 1], ((gl - 1) >> 1) & 1, wc);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint32_t kv[64];
+                    tmem_ld32_at<0>(tRow + 256, kv);   // dV
+                    tmem_ld32_at<32>(tRow + 288, kv);
+                    tmem_wait_ld();
+                    uint8_t* epi = smem + Cfg::kDSOff + ((gl + 1) & 1) * Cfg::kDSBytes;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(epi + qr * 128 + ((c ^ (qr & 7)) << 4)) =
+                            make_uint4(pack_h16<F16>(__uint_as_float(kv[8 * c + 0]), __uint_as_float(kv[8 * c + 1])),
+                                       pack_h16<F16>(__uint_as_float(kv[8 * c + 2]), __uint_as_float(kv[8 * c + 3])),
+                                       pack_h16<F16>(__uint_as_float(kv[8 * c + 4]), __uint_as_float(kv[8 * c + 5])),
+                                       pack_h16<F16>(__uint_as_float(kv[8 * c + 6]), __uint_as_float(kv[8 * c + 7])));
+                    tmem_ld32_at<0>(tRow + 320, kv);   // dK
+                    tmem_ld32_at<32>(tRow + 352, kv);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&bar.dkv_empty);  // the accumulators may take the next unit
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(epi + 128 * 128 + qr * 128 + ((c ^ (qr & 7)) << 4)) = make_uint4(
+                            pack_h16<F16>(__uint_as_float(kv[8 * c + 0]) * p.scale,
+                                          __uint_as_float(kv[8 * c + 1]) * p.scale),
+                            pack_h16<F16>(__uint_as_float(kv[8 * c + 2]) * p.scale,
+                                          __uint_as_float(kv[8 * c + 3]) * p.scale),
+                            pack_h16<F16>(__uint_as_float(kv[8 * c + 4]) * p.scale,
+                                          __uint_as_float(kv[8 * c + 5]) * p.scale),
+                            pack_h16<F16>(__uint_as_float(kv[8 * c + 6]) * p.scale,
+                                          __uint_as_float(kv[8 * c + 7]) * p.scale));
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bar.epi_staged);
+                    if (issuer) {
+                        ok = mbar_wait(&bar.epi_staged, n & 1, wc);
+                        if (ok) {
+                            tma_store_4d(&tm_dv, epi, 0, w.k0, w.h, w.b);
+                            tma_store_4d(&tm_dk, epi + 128 * 128, 0, w.k0, w.h, w.b);
+                            bulk_commit();
+                            bulk_wait_read0();
+                            mbar_arrive(&bar.epi_free);
+                        }
+                    }
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
                 ok = mbar_wait(&bar.dq_full, gt & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -988,56 +1046,8 @@ __global__ void __launch_bounds__(512, 1)
                         mbar_arrive(&bar.dq_free);
                     }
                 }
+                ok = __all_sync(0xffffffffu, ok);
             }
-            if (!ok) break;
-            // unit epilogue (thread = key row): dV and scale * dK leave through shared memory
-            // and TMA stores, so the P^T / dS^T warps go straight on to the next unit. The
-            // staging area is the dS buffer of the unit's second-to-last tile, which its dQ
-            // product has read; the next tile to write that buffer is the next unit's first,
-            // after these stores have read it (epi_free). Rows beyond N are clipped by the maps.
-            const int gl = gt - 1;  // this unit's last tile
-            ok = mbar_wait(&bar.kv_done, n & 1, wc);
-            if (gl >= 1) ok = ok && mbar_wait(&bar.dq_done[(gl - 1) & 1], ((gl - 1) >> 1) & 1, wc);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t kv[64];
-            tmem_ld32_at<0>(tRow + 256, kv);   // dV
-            tmem_ld32_at<32>(tRow + 288, kv);
-            tmem_wait_ld();
-            uint8_t* epi = smem + Cfg::kDSOff + ((gl + 1) & 1) * Cfg::kDSBytes;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(epi + qr * 128 + ((c ^ (qr & 7)) << 4)) =
-                    make_uint4(pack_h16<F16>(__uint_as_float(kv[8 * c + 0]), __uint_as_float(kv[8 * c + 1])),
-                               pack_h16<F16>(__uint_as_float(kv[8 * c + 2]), __uint_as_float(kv[8 * c + 3])),
-                               pack_h16<F16>(__uint_as_float(kv[8 * c + 4]), __uint_as_float(kv[8 * c + 5])),
-                               pack_h16<F16>(__uint_as_float(kv[8 * c + 6]), __uint_as_float(kv[8 * c + 7])));
-            tmem_ld32_at<0>(tRow + 320, kv);   // dK
-            tmem_ld32_at<32>(tRow + 352, kv);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&bar.dkv_empty);  // the accumulators may take the next unit
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(epi + 128 * 128 + qr * 128 + ((c ^ (qr & 7)) << 4)) = make_uint4(
-                    pack_h16<F16>(__uint_as_float(kv[8 * c + 0]) * p.scale, __uint_as_float(kv[8 * c + 1]) * p.scale),
-                    pack_h16<F16>(__uint_as_float(kv[8 * c + 2]) * p.scale, __uint_as_float(kv[8 * c + 3]) * p.scale),
-                    pack_h16<F16>(__uint_as_float(kv[8 * c + 4]) * p.scale, __uint_as_float(kv[8 * c + 5]) * p.scale),
-                    pack_h16<F16>(__uint_as_float(kv[8 * c + 6]) * p.scale, __uint_as_float(kv[8 * c + 7]) * p.scale));
-            fence_proxy_async_smem();
-            mbar_arrive(&bar.epi_staged);
-            if (issuer) {
-                ok = mbar_wait(&bar.epi_staged, n & 1, wc);
-                if (ok) {
-                    tma_store_4d(&tm_dv, epi, 0, w.k0, w.h, w.b);
-                    tma_store_4d(&tm_dk, epi + 128 * 128, 0, w.k0, w.h, w.b);
-                    bulk_commit();
-                    bulk_wait_read0();
-                    mbar_arrive(&bar.epi_free);
-                }
-            }
-            ok = __all_sync(0xffffffffu, ok);
         }
         if (issuer) bulk_wait0();  // reductions and stores complete before the CTA exits
     }
