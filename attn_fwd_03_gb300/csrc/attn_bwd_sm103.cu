@@ -510,10 +510,10 @@ __global__ void __launch_bounds__(384, 1)
 // stores.
 //
 // Warps (16): 0-7 P^T / dS^T (two warpgroups, 32 queries of each half each),
-// 8 TMA producer, 9 and 10 MMA issuers, 11 idle, 12-15 dQ drain and the
-// units' dV / dK epilogues. The drain and the epilogues have their own
-// warpgroup so the P^T / dS^T warps move on to the next half, and the next
-// unit, at once.
+// 8 TMA producer, 9 and 10 MMA issuers, 11 the TMA reductions of dQ and the
+// stores of dV / dK, 12-15 dQ drain and the units' dV / dK epilogues. The drain
+// and the epilogues have their own warpgroup so the P^T / dS^T warps move on to
+// the next half, and the next unit, at once.
 // ============================================================================
 template <bool MASK>
 struct Bwd64Cfg {
@@ -934,14 +934,11 @@ __global__ void __launch_bounds__(512, 1)
         // ------------------------------------------------ dQ drain (thread = query row of the tile),
         // and each unit's dV / dK epilogue
         // scale * dQ goes to shared memory in the 128-byte-swizzled layout of the
-        // accumulator's tensor map (box bx = columns 32 bx .. 32 bx + 31), and one
-        // thread adds both boxes into the fp32 accumulator with TMA reductions.
-        // Rows beyond N are clipped by the tensor map.
+        // accumulator's tensor map (box bx = columns 32 bx .. 32 bx + 31), and warp 11
+        // adds both boxes into the fp32 accumulator with TMA reductions.
         const int qr = (warp & 3) * 32 + lane;
         const uint32_t tRow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         uint8_t* stg = smem + Cfg::kStgOff;
-        const bool issuer = threadIdx.x == 384;
-        if (issuer) prefetch_tmap(&tm_dq);
         bool ok = true;
         int gt = 0, n = 0;
         for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku), ++n) {
@@ -991,19 +988,7 @@ __global__ void __launch_bounds__(512, 1)
                             pack_h16<F16>(__uint_as_float(kv[8 * c + 6]) * p.scale,
                                           __uint_as_float(kv[8 * c + 7]) * p.scale));
                     fence_proxy_async_smem();
-                    mbar_arrive(&bar.epi_staged);
-                    if (issuer) {
-                        ok = mbar_wait(&bar.epi_staged, n & 1, wc);
-                        if (ok) {
-                            tma_store_4d(&tm_dv, epi, 0, w.k0, w.h, w.b);
-                            tma_store_4d(&tm_dk, epi + 128 * 128, 0, w.k0, w.h, w.b);
-                            bulk_commit();
-                            bulk_wait_read0();
-                            mbar_arrive(&bar.epi_free);
-                        }
-                    }
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
+                    mbar_arrive(&bar.epi_staged);  // warp 11 stores them
                 }
                 ok = mbar_wait(&bar.dq_full, gt & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
@@ -1035,21 +1020,55 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bar.dq_staged);
-                if (issuer) {
-                    ok = mbar_wait(&bar.dq_staged, gt & 1, wc);
-                    if (ok) {
-                        const int q0 = (w.i_begin + it) * BQ;
-                        tma_reduce_add_4d(&tm_dq, stg, 0, q0, w.h, w.b);
-                        tma_reduce_add_4d(&tm_dq, stg + BQ * 128, 32, q0, w.h, w.b);
-                        bulk_commit();
-                        bulk_wait_read0();
-                        mbar_arrive(&bar.dq_free);
-                    }
-                }
-                ok = __all_sync(0xffffffffu, ok);
             }
         }
-        if (issuer) bulk_wait0();  // reductions and stores complete before the CTA exits
+    } else if (warp == 11) {
+        // ------------------------------------------------ bulk copies out of shared memory
+        // One elected lane (always the same one: the warp is converged) adds each staged dQ
+        // tile into the fp32 accumulator and stores each unit's dV / dK, in the order the
+        // drain stages them (a unit's epilogue before its last dQ tile), and waits for each
+        // copy to read shared memory before handing the area back. Keeping those waits here
+        // keeps them off the drain warpgroup. Rows beyond N are clipped by the tensor maps.
+        uint8_t* stg = smem + Cfg::kStgOff;
+        if (elect_one()) {
+            prefetch_tmap(&tm_dq);
+            prefetch_tmap(&tm_dk);
+            prefetch_tmap(&tm_dv);
+        }
+        __syncwarp();
+        bool ok = true;
+        int gt = 0, n = 0;
+        for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku), ++n) {
+            const Unit64 w = unit64(p, u);
+            for (int it = 0; it < w.n_it && ok; ++it, ++gt) {
+                if (it == w.n_it - 1) {
+                    ok = mbar_wait_warp(&bar.epi_staged, n & 1, wc);
+                    if (!ok) break;
+                    uint8_t* epi = smem + Cfg::kDSOff + ((gt + 1) & 1) * Cfg::kDSBytes;
+                    if (elect_one()) {
+                        tma_store_4d(&tm_dv, epi, 0, w.k0, w.h, w.b);
+                        tma_store_4d(&tm_dk, epi + 128 * 128, 0, w.k0, w.h, w.b);
+                        bulk_commit();
+                        bulk_wait_read0();
+                        mbar_arrive(&bar.epi_free);
+                    }
+                    __syncwarp();
+                }
+                ok = mbar_wait_warp(&bar.dq_staged, gt & 1, wc);
+                if (!ok) break;
+                if (elect_one()) {
+                    const int q0 = (w.i_begin + it) * BQ;
+                    tma_reduce_add_4d(&tm_dq, stg, 0, q0, w.h, w.b);
+                    tma_reduce_add_4d(&tm_dq, stg + BQ * 128, 32, q0, w.h, w.b);
+                    bulk_commit();
+                    bulk_wait_read0();
+                    mbar_arrive(&bar.dq_free);
+                }
+                __syncwarp();
+            }
+        }
+        if (elect_one()) bulk_wait0();  // reductions and stores complete before the CTA exits
+        __syncwarp();
     }
 
     tc_fence_before();
