@@ -536,12 +536,11 @@ struct __align__(8) Bwd64Barriers {
     uint64_t kv_full[2];              // per K/V buffer
     uint64_t kv_free[2];              // per K/V buffer: both issuers done with its unit's K and V
     uint64_t dkv_empty;               // the drain warpgroup has read this unit's dV and dK
-    uint64_t epi_staged, epi_free;    // dV / dK tile staged in shared memory / TMA store done reading it
     uint64_t st_full[2], st_empty[2];
     uint64_t s_full[3], ds_ready[3];  // per S slot
     uint64_t dp_loaded[2];            // per dP slot: the warpgroups have loaded dP^T
     uint64_t dq_full, dq_empty, kv_done, drain[2];
-    uint64_t dq_staged, dq_free;      // dQ staging in shared memory filled / free again
+    uint64_t dq_staged, dq_free;      // staging area filled (a dQ tile, or a unit's dV / dK) / free again
     uint64_t buf_free[3];             // per S slot: dV / dK of its half done reading it
     uint64_t dq_done[2];              // dQ of the tile in a dS buffer done reading it
     uint32_t tmem_base;
@@ -609,8 +608,6 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&bar.kv_free[i], 2);
         }
         mbar_init(&bar.dkv_empty, 128);
-        mbar_init(&bar.epi_staged, 128);
-        mbar_init(&bar.epi_free, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bar.st_full[i], 1);
             mbar_init(&bar.st_empty[i], 1);
@@ -909,11 +906,6 @@ __global__ void __launch_bounds__(512, 1)
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
-                if (hl == 0 && n > 0) {  // the previous unit's dV / dK stores have read this dS buffer
-                    ok = mbar_wait(&bar.epi_free, (n - 1) & 1, wc);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
-                }
                 // dS row kr, queries ql0 .. ql0+31 of tile buffer (gt & 1): box hf, chunks 4g .. 4g+3
                 uint8_t* box = smem + Cfg::kDSOff + (gt & 1) * Cfg::kDSBytes + hf * (128 * 128) + kr * 128;
 #pragma unroll
@@ -933,29 +925,26 @@ __global__ void __launch_bounds__(512, 1)
     else if (warp >= 12) {
         // ------------------------------------------------ dQ drain (thread = query row of the tile),
         // and each unit's dV / dK epilogue
-        // scale * dQ goes to shared memory in the 128-byte-swizzled layout of the
-        // accumulator's tensor map (box bx = columns 32 bx .. 32 bx + 31), and warp 11
-        // adds both boxes into the fp32 accumulator with TMA reductions.
+        // Both leave through one shared-memory staging area, in the 128-byte-swizzled layout
+        // of the TMA maps, and warp 11 copies them out: scale * dQ (box bx = columns 32 bx ..
+        // 32 bx + 31) is added into the fp32 accumulator, dV and scale * dK are stored. The
+        // area is used in a fixed order, the same for both sides: each dQ tile, with a unit's
+        // epilogue just before its last one. Use k waits until use k-1 has been read.
         const int qr = (warp & 3) * 32 + lane;
         const uint32_t tRow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         uint8_t* stg = smem + Cfg::kStgOff;
         bool ok = true;
-        int gt = 0, n = 0;
+        int gt = 0, n = 0, use = 0;
         for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku), ++n) {
             const Unit64 w = unit64(p, u);
             for (int it = 0; it < w.n_it && ok; ++it, ++gt) {
                 if (it == w.n_it - 1) {
-                    // unit epilogue (thread = key row), taken before the unit's last dQ: dV and
-                    // dK are complete once their last products are (kv_done), and reading them
-                    // out here lets the next unit's gradients start while that dQ is still in
-                    // the tensor core. They leave through shared memory and TMA stores, so the
-                    // P^T / dS^T warps go straight on to the next unit. The staging area is the
-                    // dS buffer of the unit's second-to-last tile, which its dQ product has
-                    // read; the next tile to write that buffer is the next unit's first, after
-                    // these stores have read it (epi_free). Rows beyond N are clipped by the maps.
-                    const int gl = gt;  // this unit's last tile
+                    // unit epilogue (thread = key row), before the unit's last dQ: dV and dK are
+                    // complete once their last products are (kv_done), and reading them out
+                    // here lets the next unit's gradients start while that dQ is still in the
+                    // tensor core. The P^T / dS^T warps go straight on to the next unit.
                     ok = mbar_wait(&bar.kv_done, n & 1, wc);
-                    if (gl >= 1) ok = ok && mbar_wait(&bar.dq_done[(gl - 1) & 1], ((gl - 1) >> 1) & 1, wc);
+                    if (use > 0) ok = ok && mbar_wait(&bar.dq_free, (use - 1) & 1, wc);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
@@ -963,10 +952,9 @@ __global__ void __launch_bounds__(512, 1)
                     tmem_ld32_at<0>(tRow + 256, kv);   // dV
                     tmem_ld32_at<32>(tRow + 288, kv);
                     tmem_wait_ld();
-                    uint8_t* epi = smem + Cfg::kDSOff + ((gl + 1) & 1) * Cfg::kDSBytes;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(epi + qr * 128 + ((c ^ (qr & 7)) << 4)) =
+                        *reinterpret_cast<uint4*>(stg + qr * 128 + ((c ^ (qr & 7)) << 4)) =
                             make_uint4(pack_h16<F16>(__uint_as_float(kv[8 * c + 0]), __uint_as_float(kv[8 * c + 1])),
                                        pack_h16<F16>(__uint_as_float(kv[8 * c + 2]), __uint_as_float(kv[8 * c + 3])),
                                        pack_h16<F16>(__uint_as_float(kv[8 * c + 4]), __uint_as_float(kv[8 * c + 5])),
@@ -978,7 +966,7 @@ __global__ void __launch_bounds__(512, 1)
                     mbar_arrive(&bar.dkv_empty);  // the accumulators may take the next unit
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(epi + 128 * 128 + qr * 128 + ((c ^ (qr & 7)) << 4)) = make_uint4(
+                        *reinterpret_cast<uint4*>(stg + 128 * 128 + qr * 128 + ((c ^ (qr & 7)) << 4)) = make_uint4(
                             pack_h16<F16>(__uint_as_float(kv[8 * c + 0]) * p.scale,
                                           __uint_as_float(kv[8 * c + 1]) * p.scale),
                             pack_h16<F16>(__uint_as_float(kv[8 * c + 2]) * p.scale,
@@ -988,7 +976,8 @@ __global__ void __launch_bounds__(512, 1)
                             pack_h16<F16>(__uint_as_float(kv[8 * c + 6]) * p.scale,
                                           __uint_as_float(kv[8 * c + 7]) * p.scale));
                     fence_proxy_async_smem();
-                    mbar_arrive(&bar.epi_staged);  // warp 11 stores them
+                    mbar_arrive(&bar.dq_staged);  // warp 11 stores them
+                    ++use;
                 }
                 ok = mbar_wait(&bar.dq_full, gt & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
@@ -1000,8 +989,8 @@ __global__ void __launch_bounds__(512, 1)
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&bar.dq_empty);
-                if (gt > 0) {  // the previous tile's reduction has finished reading the staging area
-                    ok = mbar_wait(&bar.dq_free, (gt - 1) & 1, wc);
+                if (use > 0) {  // the previous use of the staging area has been read
+                    ok = mbar_wait(&bar.dq_free, (use - 1) & 1, wc);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
@@ -1020,15 +1009,15 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bar.dq_staged);
+                ++use;
             }
         }
     } else if (warp == 11) {
-        // ------------------------------------------------ bulk copies out of shared memory
-        // One elected lane (always the same one: the warp is converged) adds each staged dQ
-        // tile into the fp32 accumulator and stores each unit's dV / dK, in the order the
-        // drain stages them (a unit's epilogue before its last dQ tile), and waits for each
-        // copy to read shared memory before handing the area back. Keeping those waits here
-        // keeps them off the drain warpgroup. Rows beyond N are clipped by the tensor maps.
+        // ------------------------------------------------ bulk copies out of the staging area
+        // One elected lane (always the same one: the warp is converged) copies each use of
+        // the staging area out, in the drain's order, and waits for the copy to read shared
+        // memory before handing the area back. Keeping those waits here keeps them off the
+        // drain warpgroup. Rows beyond N are clipped by the tensor maps.
         uint8_t* stg = smem + Cfg::kStgOff;
         if (elect_one()) {
             prefetch_tmap(&tm_dq);
@@ -1037,24 +1026,24 @@ __global__ void __launch_bounds__(512, 1)
         }
         __syncwarp();
         bool ok = true;
-        int gt = 0, n = 0;
-        for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku), ++n) {
+        int use = 0;
+        for (int ku = 0, u = bwd_unit_at(0); u < p.num_units && ok; u = bwd_unit_at(++ku)) {
             const Unit64 w = unit64(p, u);
-            for (int it = 0; it < w.n_it && ok; ++it, ++gt) {
-                if (it == w.n_it - 1) {
-                    ok = mbar_wait_warp(&bar.epi_staged, n & 1, wc);
+            for (int it = 0; it < w.n_it && ok; ++it) {
+                if (it == w.n_it - 1) {  // the unit's dV and dK
+                    ok = mbar_wait_warp(&bar.dq_staged, use & 1, wc);
                     if (!ok) break;
-                    uint8_t* epi = smem + Cfg::kDSOff + ((gt + 1) & 1) * Cfg::kDSBytes;
                     if (elect_one()) {
-                        tma_store_4d(&tm_dv, epi, 0, w.k0, w.h, w.b);
-                        tma_store_4d(&tm_dk, epi + 128 * 128, 0, w.k0, w.h, w.b);
+                        tma_store_4d(&tm_dv, stg, 0, w.k0, w.h, w.b);
+                        tma_store_4d(&tm_dk, stg + 128 * 128, 0, w.k0, w.h, w.b);
                         bulk_commit();
                         bulk_wait_read0();
-                        mbar_arrive(&bar.epi_free);
+                        mbar_arrive(&bar.dq_free);
                     }
                     __syncwarp();
+                    ++use;
                 }
-                ok = mbar_wait_warp(&bar.dq_staged, gt & 1, wc);
+                ok = mbar_wait_warp(&bar.dq_staged, use & 1, wc);
                 if (!ok) break;
                 if (elect_one()) {
                     const int q0 = (w.i_begin + it) * BQ;
@@ -1065,6 +1054,7 @@ __global__ void __launch_bounds__(512, 1)
                     mbar_arrive(&bar.dq_free);
                 }
                 __syncwarp();
+                ++use;
             }
         }
         if (elect_one()) bulk_wait0();  // reductions and stores complete before the CTA exits
