@@ -26,6 +26,12 @@
  *    message from attn_last_error(). Errors inside a kernel (a bounded wait
  *    that ran out) are recorded in a device error word and reported by the
  *    next attn_status() on that device.
+ *  - Launch chaining: the tensor-core kernels and the backward's and decode's
+ *    helper kernels are launched with programmatic stream serialization.
+ *    Such a kernel may start its on-chip set-up while the kernel before it
+ *    on the stream is still finishing. Before it touches device memory it
+ *    waits until that kernel has completed and its writes are visible. Stream
+ *    order is therefore kept exactly; only the launch gap shrinks.
  *  - Values: Q, K, V and the mask must be finite, except that mask entries
  *    may be -inf ("masked"). NaN or +inf inputs give undefined results (the
  *    pages' row recurrence rejects them up front: "Explain FlashAttention and
