@@ -1,0 +1,82 @@
+"""Host-side logic of bench.py that needs no GPU: the lookup of captured DRAM traffic, which
+the bench line may only report while the kernel's sources are the ones that were profiled."""
+import hashlib
+import json
+
+import pytest
+
+import bench
+
+
+def _setup(root, src_text="kernel body v1\n", entries=None):
+    (root / "profiles").mkdir()
+    (root / "src").mkdir()
+    src = root / "src" / "k.cu"
+    src.write_text(src_text)
+    digest = hashlib.sha256(src_text.encode()).hexdigest()
+    if entries is None:
+        entries = [{"kernel": "main_kernel", "workload": "w", "sources": {"src/k.cu": digest},
+                    "dram_bytes_read": 1000, "dram_bytes_write": 24}]
+    (root / "profiles" / "dram_traffic.json").write_text(json.dumps({"entries": entries}))
+    return src
+
+
+@pytest.fixture
+def root(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    return tmp_path
+
+
+def test_traffic_reported_while_sources_match(root):
+    _setup(root)
+    assert bench.captured_traffic("main_kernel", "w") == 1024
+
+
+def test_traffic_stale_after_a_source_edit(root):
+    src = _setup(root)
+    src.write_text("kernel body v2\n")
+    assert bench.captured_traffic("main_kernel", "w") is None
+
+
+def test_traffic_stale_when_a_source_is_missing(root):
+    src = _setup(root)
+    src.unlink()
+    assert bench.captured_traffic("main_kernel", "w") is None
+
+
+def test_traffic_needs_the_same_kernel_and_workload(root):
+    _setup(root)
+    assert bench.captured_traffic("main_kernel", "other") is None
+    assert bench.captured_traffic("other_kernel", "w") is None
+
+
+def test_traffic_every_listed_source_must_match(root):
+    src = _setup(root)
+    second = root / "src" / "h.cuh"
+    second.write_text("header\n")
+    entries = [{"kernel": "main_kernel", "workload": "w",
+                "sources": {"src/k.cu": hashlib.sha256(src.read_bytes()).hexdigest(),
+                            "src/h.cuh": hashlib.sha256(b"older header\n").hexdigest()},
+                "dram_bytes_read": 1, "dram_bytes_write": 1}]
+    (root / "profiles" / "dram_traffic.json").write_text(json.dumps({"entries": entries}))
+    assert bench.captured_traffic("main_kernel", "w") is None
+
+
+def test_traffic_none_without_a_readable_file(root):
+    assert bench.captured_traffic("main_kernel", "w") is None  # no profiles/ at all
+    (root / "profiles").mkdir()
+    (root / "profiles" / "dram_traffic.json").write_text("{ not json")
+    assert bench.captured_traffic("main_kernel", "w") is None
+
+
+def test_committed_entries_name_existing_sources_and_summaries():
+    # every committed entry points at files of this repository and carries both byte counts
+    import os
+    with open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")) as f:
+        doc = json.load(f)
+    assert doc["entries"]
+    for e in doc["entries"]:
+        assert e["dram_bytes_read"] > 0 and e["dram_bytes_write"] >= 0
+        for rel in e["sources"]:
+            assert os.path.exists(os.path.join(bench.ROOT, rel)), rel
+        assert os.path.exists(os.path.join(bench.ROOT, e["summary"])), e["summary"]
