@@ -80,3 +80,42 @@ def test_committed_entries_name_existing_sources_and_summaries():
         for rel in e["sources"]:
             assert os.path.exists(os.path.join(bench.ROOT, rel)), rel
         assert os.path.exists(os.path.join(bench.ROOT, e["summary"])), e["summary"]
+
+
+def _clock_line(sm, mx=2070, hw="Not Active", hwt="Not Active", swt="Not Active", cap="Not Active"):
+    return f"0, {sm}, {mx}, 812.5, 0x0000000000000000, {hw}, {hwt}, {swt}, {cap}"
+
+
+def test_clock_summary_median_and_no_reasons():
+    c = bench.ClockSampler(0)
+    c.lines = [_clock_line(2070), _clock_line(2055), _clock_line(2070)]
+    c.first = 0
+    s = c.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3}
+
+
+def test_clock_summary_reports_throttle_reasons():
+    c = bench.ClockSampler(0)
+    c.lines = [_clock_line(1980, cap="Active"), _clock_line(1500, hwt="Active"), _clock_line(2070)]
+    c.first = 0
+    assert c.summary()["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_clock_summary_counts_only_the_timed_region():
+    # samples before the timed region are left out, except the last one before it began
+    c = bench.ClockSampler(0)
+    c.lines = [_clock_line(900, hw="Active"), _clock_line(1000), _clock_line(2070), _clock_line(2070)]
+    c.first = 2
+    s = c.summary()
+    assert s["samples"] == 3 and s["reasons"] == [] and s["sm_mhz"] == 2070.0
+
+
+def test_clock_summary_skips_unreadable_rows():
+    c = bench.ClockSampler(0)
+    c.lines = ["0, [N/A], [N/A], [N/A], 0x0, Not Active, Not Active, Not Active, Not Active", "garbage",
+               _clock_line(2040)]
+    c.first = 0
+    s = c.summary()
+    assert s["samples"] == 1 and s["sm_mhz"] == 2040.0
+    empty = bench.ClockSampler(0)
+    assert empty.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
