@@ -2,27 +2,27 @@
 
 Tolerances (written here once, used by every parity test):
   * bf16 inputs, fp32 accumulation: max-abs error <= 2e-2 and relative-L2
-    error <= 5e-3 on O; gradients use the same two numbers, with the max-abs
-    bound taken relative to max(1, max |reference|) because a bf16 output of
-    magnitude M cannot be closer than its own rounding step (M * 2^-9).
+    error <= 5e-3 on O (gradients: the same two numbers, below).
   * fp32 inputs: max-abs <= 1e-4 on O and LSE.
   * LSE: max-abs <= 1e-3 on finite entries; -inf entries (fully masked rows)
     must sit at exactly the same positions, and those rows of O must be 0.
   * Gradients. The backward computes D = rowsum(dO * O) from the O the forward
-    stored in bf16, as the method prescribes (the backward recomputes from
-    the stored output and statistics). Where dP - D cancels (tiny N, peaked
-    P) that storage rounding alone moves dQ and dK by more than 5e-3 of their
-    norm, so the bound is derived from it: against the pure fp64 gradient,
-        rel-L2  <= 5e-3 + 2 * delta,   max-abs <= 2e-2 * max(1, max|ref|) + 2 * delta_abs,
-    where delta / delta_abs are the relative-L2 / max-abs change the oracle
-    itself sees when it takes D from its own bf16-rounded O instead of the
-    exact one. Both come from the oracle alone; for non-degenerate shapes
-    delta is ~1e-3.
+    stored (bf16 or half), as the method prescribes: it recomputes from the
+    stored output and the saved row statistics. The oracle for that method is
+    the fp64 gradient with D taken from the oracle's own O rounded to the
+    storage dtype (o_storage="bf16" / "f16"). Gradients are held to the same
+    two numbers as O against it: rel-L2 <= 5e-3 and max-abs <= 2e-2 *
+    max(1, max|ref|). The max-abs bound scales with the largest reference
+    value because a bf16 number of magnitude M in [2^e, 2^(e+1)) is only
+    representable to half a unit in the last place, 2^(e-8), which exceeds
+    2e-2 once M > 5.12 (the large-score workload's dQ reaches ~21); at
+    max|ref| <= 1 the bound is the plain 2e-2. The distance to the pure fp64
+    gradient (D from the exact O) is returned for reporting, not asserted.
   * IEEE half inputs (an extension; no tolerance is stated for them). Half
     keeps 10 fraction bits against bf16's 7, so every rounding in the path
     (inputs, P, dS, O, dQ/dK/dV) is 8x finer; the bf16 bounds are scaled by
-    1/8 and rounded up: max-abs <= 4e-3 and rel-L2 <= 1e-3 (gradients: the
-    same derived allowance, with delta taken from a half-rounded O).
+    1/8 and rounded up: max-abs <= 4e-3 and rel-L2 <= 1e-3 (gradients against
+    the half-stored oracle, o_storage="f16").
 """
 from __future__ import annotations
 
@@ -92,17 +92,42 @@ def assert_masked_rows_zero(o, lse_ref):
         assert np.all(o[dead] == 0.0), "fully masked rows of O must be exactly 0"
 
 
-def assert_grad(name, got, pure, stored):
-    """Gradient check with the stored-output allowance described above."""
+def assert_grad(name, got, stored, pure=None):
+    """Gradient check against the stored-output oracle, with the bounds above.
+
+    Returns {"stored": (max_abs, rel_l2)} and, when `pure` is given, also
+    {"pure": (max_abs, rel_l2)}: the distance to the gradient with D from the
+    exact O, reported only."""
     atol, rtol = _bounds(got.dtype if isinstance(got, torch.Tensor) else None)
-    g, w, st = to64(got), to64(pure), to64(stored)
-    delta_abs, delta = errors(st, w)
+    g, w = to64(got), to64(stored)
     max_abs, rel = errors(g, w)
-    bound_abs = atol * max(1.0, float(np.max(np.abs(w))) if w.size else 1.0) + 2 * delta_abs
-    bound_rel = rtol + 2 * delta
-    assert max_abs <= bound_abs and rel <= bound_rel, \
-        f"{name}: max-abs {max_abs:.3e} (bound {bound_abs:.3e}), rel-L2 {rel:.3e} (bound {bound_rel:.3e})"
-    return max_abs, rel
+    bound_abs = atol * max(1.0, float(np.max(np.abs(w))) if w.size else 1.0)
+    assert max_abs <= bound_abs and rel <= rtol, \
+        f"{name}: max-abs {max_abs:.3e} (bound {bound_abs:.3e}), rel-L2 {rel:.3e} (bound {rtol:.1e})"
+    out = {"stored": (max_abs, rel)}
+    if pure is not None:
+        out["pure"] = errors(g, to64(pure))
+    return out
+
+
+def stored_forward(inp, causal, scale, device="cuda"):
+    """The oracle's O rounded to the input dtype (what a forward stores) and its LSE in
+    fp32, as device tensors: the saved outputs a backward consumes, from the oracle
+    alone. Feeding these to the CUDA backward makes it compute the very function the
+    stored-output oracle defines."""
+    from oracle import ref
+    mask = inp.get("mask")
+    O, L = ref.attention_forward(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), scale, causal,
+                                 None if mask is None else to64(mask))
+    dt = inp["q"].dtype
+    rnd = ref.round_f16 if dt == torch.float16 else ref.round_bf16
+    o = torch.from_numpy(rnd(O)).to(dt).to(device)
+    lse = torch.from_numpy(L).to(torch.float32).to(device)
+    return o, lse
+
+
+def storage_of(dtype):
+    return "f16" if dtype == torch.float16 else "bf16"
 
 
 def padded_mask(mask: torch.Tensor, device=None) -> torch.Tensor:

@@ -10,7 +10,7 @@ import torch
 
 import workloads as W
 from oracle import ref
-from parity_util import assert_close_bf16, assert_grad, padded_mask, to64
+from parity_util import assert_close_bf16, assert_grad, padded_mask, storage_of, stored_forward, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -31,9 +31,14 @@ def _dev(x):
     return x.to("cuda")
 
 
-def _run(A, inp, causal, scale, entry="attn_bwd_deterministic"):
+def _run(A, inp, causal, scale, entry="attn_bwd_deterministic", saved="oracle"):
+    """The backward on the oracle's saved O and LSE (saved="oracle": the function the
+    stored-output oracle defines) or on the kernel forward's own (saved="kernel")."""
     q, k, v, mask, do = (_dev(inp.get(n)) for n in ("q", "k", "v", "mask", "do"))
-    o, lse = A.attn_fwd(q, k, v, scale=scale, causal=causal, mask=mask)
+    if saved == "oracle":
+        o, lse = stored_forward(inp, causal, scale)
+    else:
+        o, lse = A.attn_fwd(q, k, v, scale=scale, causal=causal, mask=mask)
     grads = getattr(A, entry)(q, k, v, o, lse, do, scale=scale, causal=causal, mask=mask)
     torch.cuda.synchronize()
     assert A.attn_status() == A.ATTN_OK, A.last_error()
@@ -44,10 +49,10 @@ def _check(grads, inp, causal, scale):
     mask = inp.get("mask")
     args = (to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), to64(inp["do"]), scale, causal,
             None if mask is None else to64(mask))
-    stored = ref.attention_backward(*args, o_storage="f16" if inp["q"].dtype == torch.float16 else "bf16")
+    stored = ref.attention_backward(*args, o_storage=storage_of(inp["q"].dtype))
     pure = ref.attention_backward(*args)
     for i, (name, g) in enumerate(zip(("dQ", "dK", "dV"), grads)):
-        assert_grad(name, g, pure[i], stored[i])
+        assert_grad(name, g, stored[i], pure[i])
 
 
 def _inputs(shape, seed, dtype=torch.bfloat16):
@@ -63,6 +68,7 @@ def test_reduced_workloads(A, idx, shape):
     w = W.WORKLOADS[idx]
     inp = W.make_inputs(w, with_grad=True, shape=shape)
     _check(_run(A, inp, w.causal, w.scale), inp, w.causal, w.scale)
+    _check(_run(A, inp, w.causal, w.scale, saved="kernel"), inp, w.causal, w.scale)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -147,7 +153,7 @@ def test_empty_problem(A):
 def test_full_size_sampled(A, idx):
     w = W.WORKLOADS[idx]
     inp = W.make_inputs(w)
-    dq, dk, dv = _run(A, inp, w.causal, w.scale)
+    dq, dk, dv = _run(A, inp, w.causal, w.scale, saved="kernel")
     b, h = w.B - 1, w.H // 2
     r = np.random.default_rng(300 + idx)
     rows = np.array(sorted(set(r.choice(w.N, size=48, replace=False).tolist()) | {0, w.N - 1, 127, 128}))
@@ -157,7 +163,7 @@ def test_full_size_sampled(A, idx):
     pure = ref.backward_head(*hargs, q_rows=rows, k_rows=rows)
     stored = ref.backward_head(*hargs, q_rows=rows, k_rows=rows, o_storage="bf16")
     for i, (name, g) in enumerate((("dQ", dq), ("dK", dk), ("dV", dv))):
-        assert_grad(name, g[b, h, rows], pure[i], stored[i])
+        assert_grad(name, g[b, h, rows], stored[i], pure[i])
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()
 

@@ -14,7 +14,7 @@ import torch
 import workloads as W
 from oracle import ref
 from parity_util import (assert_close_bf16, assert_close_f32, assert_grad, assert_lse, assert_masked_rows_zero,
-                         padded_mask, to64)
+                         padded_mask, storage_of, stored_forward, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -69,12 +69,20 @@ def _check_fwd(o, lse, inp, causal, scale, f32=False):
 
 
 def _check_bwd(grads, inp, causal, scale):
+    """dQ, dK, dV against the oracle whose D comes from its own stored (bf16 / half) O."""
     args = (to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), to64(inp["do"]), scale, causal,
             _oracle_mask(inp.get("mask")))
-    stored = ref.attention_backward(*args, o_storage="f16" if inp["q"].dtype == torch.float16 else "bf16")
+    stored = ref.attention_backward(*args, o_storage=storage_of(inp["q"].dtype))
     pure = ref.attention_backward(*args)
-    for i, (name, g) in enumerate(zip(("dQ", "dK", "dV"), grads)):
-        assert_grad(name, g, pure[i], stored[i])
+    return {name: assert_grad(name, g, stored[i], pure[i]) for i, (name, g) in enumerate(zip(("dQ", "dK", "dV"), grads))}
+
+
+def _bwd_from_oracle_outputs(A, inp, causal, scale):
+    """The backward run on the O and LSE the oracle saves (O rounded to the input dtype,
+    LSE in fp32): it then computes exactly the function the stored-output oracle defines,
+    and every difference is the kernel's own rounding."""
+    o, lse = stored_forward(inp, causal, scale)
+    return _run_bwd(A, inp, causal, scale, o, lse)
 
 
 # --------------------------------------------------------------- small cases
@@ -98,6 +106,8 @@ def test_reduced_workloads(A, idx, shape):
     o, lse = _run_fwd(A, inp, w.causal, w.scale)
     _check_fwd(o, lse, inp, w.causal, w.scale)
     if w.backward:
+        _check_bwd(_bwd_from_oracle_outputs(A, inp, w.causal, w.scale), inp, w.causal, w.scale)
+        # and chained on the kernel's own forward outputs, against the same oracle
         _check_bwd(_run_bwd(A, inp, w.causal, w.scale, o, lse), inp, w.causal, w.scale)
 
 
@@ -109,7 +119,7 @@ def test_edge_lengths(A, d, N, causal):
     scale = 1 / math.sqrt(d)
     o, lse = _run_fwd(A, inp, causal, scale)
     _check_fwd(o, lse, inp, causal, scale)
-    _check_bwd(_run_bwd(A, inp, causal, scale, o, lse), inp, causal, scale)
+    _check_bwd(_bwd_from_oracle_outputs(A, inp, causal, scale), inp, causal, scale)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -130,7 +140,7 @@ def test_backward_several_units_per_cta(A, causal):
     scale = 1 / math.sqrt(d)
     o, lse = _run_fwd(A, inp, causal, scale)
     _check_fwd(o, lse, inp, causal, scale)
-    _check_bwd(_run_bwd(A, inp, causal, scale, o, lse), inp, causal, scale)
+    _check_bwd(_bwd_from_oracle_outputs(A, inp, causal, scale), inp, causal, scale)
 
 
 def test_bnhd_strided_layout(A):
@@ -142,7 +152,9 @@ def test_bnhd_strided_layout(A):
     o, lse = A.attn_fwd(q, k, v, causal=True, out=o)
     torch.cuda.synchronize()
     _check_fwd(o, lse, inp, True, 1 / math.sqrt(d))
-    grads = A.attn_bwd(q, k, v, o, lse, do, causal=True)
+    o_s, lse_s = stored_forward(inp, True, 1 / math.sqrt(d))
+    o.copy_(o_s)  # the oracle's saved O, in the same strided layout
+    grads = A.attn_bwd(q, k, v, o, lse_s, do, causal=True)
     torch.cuda.synchronize()
     _check_bwd(grads, inp, True, 1 / math.sqrt(d))
 
@@ -161,7 +173,7 @@ def test_additive_mask_with_masked_rows(A, per_head):
         o, lse = _run_fwd(A, inp, causal, 0.125)
         _, L = _check_fwd(o, lse, inp, causal, 0.125)
         assert np.isneginf(L[:, :, 17]).all()
-        _check_bwd(_run_bwd(A, inp, causal, 0.125, o, lse), inp, causal, 0.125)
+        _check_bwd(_bwd_from_oracle_outputs(A, inp, causal, 0.125), inp, causal, 0.125)
 
 
 def test_all_rows_masked(A):
@@ -236,7 +248,7 @@ def test_full_size_backward_sampled(A, idx):
     pure = ref.backward_head(*hargs, q_rows=rows, k_rows=rows)
     stored = ref.backward_head(*hargs, q_rows=rows, k_rows=rows, o_storage="bf16")
     for i, (name, g) in enumerate((("dQ", dq), ("dK", dk), ("dV", dv))):
-        assert_grad(name, g[b, h, rows], pure[i], stored[i])
+        assert_grad(name, g[b, h, rows], stored[i], pure[i])
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()
 
@@ -254,6 +266,7 @@ def test_fp16_reduced_workloads(A, idx, shape):
     o, lse = _run_fwd(A, inp, w.causal, w.scale)
     assert o.dtype == torch.float16
     _check_fwd(o, lse, inp, w.causal, w.scale)
+    _check_bwd(_bwd_from_oracle_outputs(A, inp, w.causal, w.scale), inp, w.causal, w.scale)
     _check_bwd(_run_bwd(A, inp, w.causal, w.scale, o, lse), inp, w.causal, w.scale)
 
 
@@ -265,7 +278,7 @@ def test_fp16_edge_lengths(A, d, N, causal):
     scale = 1 / math.sqrt(d)
     o, lse = _run_fwd(A, inp, causal, scale)
     _check_fwd(o, lse, inp, causal, scale)
-    _check_bwd(_run_bwd(A, inp, causal, scale, o, lse), inp, causal, scale)
+    _check_bwd(_bwd_from_oracle_outputs(A, inp, causal, scale), inp, causal, scale)
 
 
 def test_fp16_additive_mask(A):
@@ -279,7 +292,7 @@ def test_fp16_additive_mask(A):
     for causal in (False, True):
         o, lse = _run_fwd(A, inp, causal, 0.125)
         _check_fwd(o, lse, inp, causal, 0.125)
-        _check_bwd(_run_bwd(A, inp, causal, 0.125, o, lse), inp, causal, 0.125)
+        _check_bwd(_bwd_from_oracle_outputs(A, inp, causal, 0.125), inp, causal, 0.125)
 
 
 def test_fp16_benchmark_shape_sampled(A):
@@ -298,4 +311,4 @@ def test_fp16_benchmark_shape_sampled(A):
     pure = ref.backward_head(*hargs, q_rows=rows, k_rows=rows)
     stored = ref.backward_head(*hargs, q_rows=rows, k_rows=rows, o_storage="f16")
     for i, (name, g) in enumerate((("dQ", dq), ("dK", dk), ("dV", dv))):
-        assert_grad(name, g[b, h, rows], pure[i], stored[i])
+        assert_grad(name, g[b, h, rows], stored[i], pure[i])
