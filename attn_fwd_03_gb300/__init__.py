@@ -15,5 +15,5 @@ from ._binding import (  # noqa: F401
     ATTN_ERR_WORKSPACE, ATTN_F16, ATTN_F32, ATTN_OK, EXPORTED, LIB_PATH, AttnError, BwdParams, DecodeParams,
     Fp8Params, FwdParams, attn_bwd, attn_bwd_deterministic, attn_bwd_noalloc, attn_decode, attn_fwd, attn_fwd_fp8,
     attn_status, bwd_workspace_size, debug_set_bwd_events, debug_set_producer_stall, decode_workspace_size,
-    last_error, lib, set_wait_timeout_ns, version,
+    last_error, launch_count, launch_names, lib, set_wait_timeout_ns, version,
 )

@@ -40,7 +40,7 @@ EXPORTED = ("attn_fwd", "attn_fwd_fp8", "attn_bwd", "attn_bwd_noalloc", "attn_bw
             "attn_decode",
             "attn_decode_workspace_size", "attn_status", "attn_last_error",
             "attn_set_wait_timeout_ns", "attn_debug_set_producer_stall", "attn_debug_set_bwd_events",
-            "attn_version")
+            "attn_debug_launch_count", "attn_debug_launch_name", "attn_version")
 
 _i64x3 = ctypes.c_int64 * 3
 
@@ -123,6 +123,10 @@ def _load() -> ctypes.CDLL:
     lib.attn_debug_set_producer_stall.restype = None
     lib.attn_debug_set_bwd_events.argtypes = [ctypes.c_void_p]
     lib.attn_debug_set_bwd_events.restype = None
+    lib.attn_debug_launch_count.argtypes = []
+    lib.attn_debug_launch_count.restype = ctypes.c_uint64
+    lib.attn_debug_launch_name.argtypes = [ctypes.c_uint32]
+    lib.attn_debug_launch_name.restype = ctypes.c_char_p
     lib.attn_version.argtypes = []
     lib.attn_version.restype = ctypes.c_int32
     return lib
@@ -341,6 +345,18 @@ def debug_set_bwd_events(events=None) -> None:
         return
     handles = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
     lib.attn_debug_set_bwd_events(ctypes.cast(handles, ctypes.c_void_p))
+
+
+def launch_count() -> int:
+    """Kernels the library has launched from this host thread so far."""
+    return int(lib.attn_debug_launch_count())
+
+
+def launch_names(count: int):
+    """Symbol names of the last `count` (<= 16) kernels launched from this host thread,
+    oldest first."""
+    names = [lib.attn_debug_launch_name(i) for i in range(count)]
+    return [n.decode(errors="replace") if n is not None else None for n in reversed(names)]
 
 
 def version() -> int:

@@ -28,6 +28,10 @@ thread_local int32_t t_stall_after = 0;
 thread_local void* t_bwd_events[4] = {nullptr, nullptr, nullptr, nullptr};
 thread_local bool t_bwd_events_on = false;
 
+constexpr uint32_t kLaunchLog = 16;
+thread_local uint64_t t_launches = 0;
+thread_local const void* t_launch_fn[kLaunchLog] = {};
+
 cudaError_t record_bwd_event(int i, cudaStream_t s) {
     if (!t_bwd_events_on) return cudaSuccess;
     return cudaEventRecord(static_cast<cudaEvent_t>(t_bwd_events[i]), s);
@@ -332,6 +336,11 @@ BwdWorkspace bwd_workspace_split(const attn_bwd_params& p) {
     return BwdWorkspace{reinterpret_cast<float*>(base), reinterpret_cast<float*>(base + stats_bytes(p.fwd))};
 }
 
+void note_launch(const void* kernel) {
+    t_launch_fn[t_launches % kLaunchLog] = kernel;
+    ++t_launches;
+}
+
 // ---- helpers for entry points that supply their own workspace storage
 attn_status_t report_error(attn_status_t st, const char* fmt, ...) {
     va_list ap;
@@ -545,6 +554,16 @@ void attn_debug_set_producer_stall(int32_t kv_tiles) { t_stall_after = kv_tiles 
 void attn_debug_set_bwd_events(void* const events[4]) {
     t_bwd_events_on = events != nullptr;
     for (int i = 0; i < 4; ++i) t_bwd_events[i] = events ? events[i] : nullptr;
+}
+
+uint64_t attn_debug_launch_count(void) { return t_launches; }
+
+const char* attn_debug_launch_name(uint32_t back) {
+    if (back >= kLaunchLog || back >= t_launches) return nullptr;
+    const void* fn = t_launch_fn[(t_launches - 1 - back) % kLaunchLog];
+    const char* name = nullptr;
+    if (cudaFuncGetName(&name, fn) != cudaSuccess || !name) return "?";
+    return name;
 }
 
 int32_t attn_version(void) { return 100; }

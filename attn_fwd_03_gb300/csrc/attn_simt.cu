@@ -314,7 +314,9 @@ cudaError_t fwd_simt_launch(const SimtArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     dim3 grid((a.N + kSimtRows - 1) / kSimtRows, a.H, a.B);
     fwd_simt_kernel<T, D><<<grid, 128, smem, s>>>(a);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e == cudaSuccess) note_launch(reinterpret_cast<const void*>(fwd_simt_kernel<T, D>));
+    return e;
 }
 
 }  // namespace

@@ -21,6 +21,11 @@ struct LaunchCommon {
     int num_sms;          // SM count of the current device
 };
 
+// Records one kernel launch of the library on the calling host thread (the launch log that
+// attn_debug_launch_count / attn_debug_launch_name read back). Called once a launch has been
+// issued without error.
+void note_launch(const void* kernel);
+
 // Launches `kernel` with programmatic stream serialization, so that it may start while the
 // kernel before it in the stream still runs. Every kernel launched this way executes
 // griddepcontrol.wait before its first global memory access, which returns once the previous
@@ -39,7 +44,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e == cudaSuccess) note_launch(reinterpret_cast<const void*>(kernel));
+    return e;
 }
 
 // Tensor maps for the tcgen05 forward (built by the host API).

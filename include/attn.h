@@ -177,7 +177,12 @@ ATTN_API attn_status_t attn_bwd(const attn_bwd_params *p, void *stream);
  *  - All calls share the one array: calls that overlap on the GPU (other
  *    streams, other threads) race and give wrong gradients. Each call
  *    re-initialises everything it reads, so results do not depend on
- *    earlier calls. */
+ *    earlier calls. Calls queued back to back on one stream do not overlap:
+ *    each call's first kernel waits for the previous kernel in the stream.
+ *  - The array's address is looked up once per device and kept. The
+ *    library must not be used on a device after cudaDeviceReset() (or any
+ *    other teardown of its primary context) in the same process: the kept
+ *    address would then point at memory the runtime has released. */
 ATTN_API attn_status_t attn_bwd_noalloc(const attn_bwd_params *p, void *stream);
 
 /* The backward pass with every gradient reproducible bit for bit: the same
@@ -233,7 +238,7 @@ ATTN_API size_t attn_decode_workspace_size(const attn_decode_params *p);
 
 /* Split-KV decode: one kernel computes each split's partial (m, l, o) over
  * its key range, a second merges the splits into O and LSE. Errors as for
- * attn_fwd; nq outside 1 .. 16 returns ATTN_ERR_UNSUPPORTED. */
+ * attn_fwd; nq outside 1 .. 128 returns ATTN_ERR_UNSUPPORTED. */
 ATTN_API attn_status_t attn_decode(const attn_decode_params *p, void *stream);
 
 /* Synchronizes `stream`, then reports (and clears) the current device's
@@ -263,6 +268,19 @@ ATTN_API void attn_debug_set_producer_stall(int32_t kv_tiles);
  * void* and stay owned by the caller; the array is copied. NULL turns the
  * hook off. */
 ATTN_API void attn_debug_set_bwd_events(void *const events[4]);
+
+/* Launch log, for checking on a real system that each call runs as fused
+ * kernels ("FlashAttention", "Checking it on a real system": the profiler
+ * should show one fused attention kernel, not separate matmul, softmax and
+ * matmul launches). attn_debug_launch_count() is the number of kernels this
+ * library has launched from the calling host thread since the process
+ * started; attn_debug_launch_name(back) is the symbol name of one of the
+ * last 16 of them (back = 0 is the most recent), or NULL when `back` is out
+ * of that range. The names are the CUDA runtime's (mangled C++ names) and
+ * stay valid until the process exits. Every launch is counted once it has
+ * been issued without a launch error. */
+ATTN_API uint64_t attn_debug_launch_count(void);
+ATTN_API const char *attn_debug_launch_name(uint32_t back);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 ATTN_API int32_t attn_version(void);

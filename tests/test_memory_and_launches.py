@@ -48,26 +48,40 @@ def test_calls_allocate_nothing(A, N):
     assert per_row < 64 * 2 * 8 + 4 + 64 * 4 + 16  # bytes per (b, h, row): no N-sized factor
 
 
-def test_one_fused_kernel_per_forward_three_per_backward(A):
-    from torch.profiler import ProfilerActivity, profile
-    q, k, v, do = _inputs(2048)
-    o, lse = A.attn_fwd(q, k, v, causal=True)
-    A.attn_bwd(q, k, v, o, lse, do, causal=True)
+def _launched(A, call):
+    """Run `call` and return the names of the kernels the library launched for it, from the
+    library's own launch log (counted on the host as each launch is issued)."""
+    before = A.launch_count()
+    call()
     torch.cuda.synchronize()
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        o, lse = A.attn_fwd(q, k, v, causal=True)
-        torch.cuda.synchronize()
-    fwd = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
-    if not fwd:
-        pytest.skip("the profiler recorded no CUDA activity on this machine")
-    fwd_kernels = [n for n in fwd if "kernel" in n]
-    assert len(fwd_kernels) == 1 and "fwd_tc_kernel" in fwd_kernels[0], fwd
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    n = A.launch_count() - before
+    assert 0 <= n <= 16, n
+    return A.launch_names(n)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_one_fused_kernel_per_forward_three_per_backward(A, d):
+    q, k, v, do = _inputs(2048, d=d)
+    o, lse = torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(A.bwd_workspace_size(q), dtype=torch.uint8, device="cuda")
-    torch.cuda.synchronize()
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        A.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
-        torch.cuda.synchronize()
-    bwd = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA and "kernel" in e.name]
+    fwd = _launched(A, lambda: A.attn_fwd(q, k, v, causal=True, out=o, lse=lse))
+    assert len(fwd) == 1 and "fwd_tc_kernel" in fwd[0], fwd
+    bwd = _launched(A, lambda: A.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws))
+    main = "bwd_tc64_kernel" if d == 64 else "bwd_tc_kernel"
     assert len(bwd) == 3, bwd
-    assert "bwd_prepass_kernel" in bwd[0] and "bwd_tc64_kernel" in bwd[1] and "bwd_dq_finalize_kernel" in bwd[2], bwd
+    assert "bwd_prepass_kernel" in bwd[0] and main in bwd[1] and "bwd_dq_finalize_kernel" in bwd[2], bwd
+
+
+def test_launch_counts_of_the_other_entry_points(A):
+    q, k, v, do = _inputs(1024, d=128)
+    o, lse = A.attn_fwd(q, k, v, causal=True)
+    det = _launched(A, lambda: A.attn_bwd_deterministic(q, k, v, o, lse, do, causal=True))
+    assert len(det) == 3 and "bwd_dq_kernel" in det[2], det
+    q1 = q[:, :, -8:].contiguous()
+    dec = _launched(A, lambda: A.attn_decode(q1, k, v, causal=True))
+    assert len(dec) == 2 and "decode_tc_kernel" in dec[0] and "decode_combine_kernel" in dec[1], dec
+    f32 = [t.float() for t in (q, k, v)]
+    simt = _launched(A, lambda: A.attn_fwd(*f32, causal=True))
+    assert len(simt) == 1 and "fwd_simt_kernel" in simt[0], simt

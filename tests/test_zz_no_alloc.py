@@ -3,8 +3,8 @@ memory when they run it (an allocator callback, a plug-in whose host owns all
 memory, a fixed memory budget). It uses the library's built-in scratch array
 instead of a caller workspace, so its results must match attn_bwd's.
 
-This file is collected last on purpose: if it fails, a run that stops at the
-first failure has already run every other test.
+The file name sorts last, so a plain sequential run reaches it after the other
+tests; nothing here depends on that order, and each test passes run alone.
 """
 import math
 
@@ -43,6 +43,28 @@ def test_matches_caller_workspace_backward_on_two_calls_in_a_row(A):
             assert_close_bf16(name, g, r, relative_max=True)
         # dK and dV are reduced in a fixed order: identical bits
         assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+
+
+def test_back_to_back_calls_on_one_stream_without_synchronising(A):
+    # three different problems queued on one stream with no synchronisation in between: each
+    # call's pre-pass rewrites the shared scratch while the previous call's kernels may still be
+    # finishing, so this checks that every call waits for the one before it
+    probs = []
+    for seed, d, causal, N in ((1400, 64, True, 300), (1500, 128, False, 517), (1600, 64, False, 129)):
+        t, scale = _problem(seed, N=N, d=d)
+        o, lse = A.attn_fwd(t["q"], t["k"], t["v"], scale=scale, causal=causal)
+        want = A.attn_bwd(t["q"], t["k"], t["v"], o, lse, t["do"], scale=scale, causal=causal)
+        probs.append((t, scale, causal, o, lse, want))
+    torch.cuda.synchronize()
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    got = [A.attn_bwd_noalloc(t["q"], t["k"], t["v"], o, lse, t["do"], scale=scale, causal=causal)
+           for t, scale, causal, o, lse, _ in probs]
+    torch.cuda.synchronize()
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    for g, (_, _, _, _, _, want) in zip(got, probs):
+        for name, a, b in zip(("dQ", "dK", "dV"), g, want):
+            assert_close_bf16(name, a, b, relative_max=True)
+        assert torch.equal(g[1], want[1]) and torch.equal(g[2], want[2])
 
 
 def test_rejects_problems_beyond_the_built_in_scratch(A):
