@@ -5,21 +5,26 @@
 A step is one pass of the whole hot path over one batch of synthetic input:
 attn_fwd (O, LSE) then attn_bwd (D pre-pass, recompute kernel, dQ finalize)
 on the workload's tensors, already resident in device memory. The default
-workload is B=4 H=16 N=2048 d=64 bf16 causal forward + backward.
+workload is the largest configuration that fits one GPU: B=1 H=16 N=32768
+d=128 bf16 causal forward + backward (long context, where a materialised
+score matrix would need 32 GiB per layer).
 
 Throughput is useful attention FLOPs per second: 4 B H N^2 d per forward,
 2.5x that per backward, halved for causal ("FlashAttention", "Checking it on
 a real system"). Prints ONE JSON line on rank 0.
 
 Timing: W untimed warm-up steps, then K timed steps between a barrier and a
-device synchronize. Inputs of the default workload fit in L2, so a 256 MiB
-buffer is rewritten before every step (outside the per-step events); each
-step's fwd and bwd are bracketed by CUDA events on the launching stream.
+device synchronize. The default workload's inputs (Q, K, V, dO: 537 MB) are
+larger than L2 (129 MB); a 256 MiB buffer is also rewritten before every
+step (outside the per-step events), so smaller workloads start cold too.
+Each step's fwd and bwd are bracketed by CUDA events on the launching stream.
 Under torchrun every rank runs its own replica (weak scaling) and the max
 over ranks is reported; nothing crosses ranks except the timing reduction.
 
 --impl reference times the fp64 CPU oracle instead, on a bounded sample of
-the same workload, on rank 0's host cores.
+the same workload, on rank 0's host cores: whole heads when N <= 4096, else
+the leading 4096 x 4096 block of each sampled head (query rows and keys
+0..4095; for a causal workload exactly those rows' forward and dQ).
 """
 from __future__ import annotations
 
@@ -124,15 +129,29 @@ class ClockSampler:
 
 
 # -------------------------------------------------------------- oracle arm
-def oracle_sample(w: W.Workload, budget_s: float, max_heads=None):
-    """Time the fp64 oracle (forward + backward) on whole heads until the
-    budget is used; returns (seconds, flops of the sampled heads, heads)."""
+SAMPLE_ROWS = 4096
+
+
+def oracle_sample(w: W.Workload, budget_s: float, max_heads=None, inp=None):
+    """Time the fp64 oracle (forward + backward) on sampled heads of the workload until the
+    budget is used; returns (seconds, flops of the sample, heads, rows per head).
+
+    A sampled head is a whole head when N <= SAMPLE_ROWS, else its leading SAMPLE_ROWS x
+    SAMPLE_ROWS block: query rows and keys 0 .. SAMPLE_ROWS-1 of the workload's own tensors.
+    For a causal workload those query rows see only those keys, so the block's forward and dQ
+    are exactly the workload's; its dK and dV hold those rows' share. FLOPs are counted for
+    the block as for a problem of that length (4 n^2 d, x3.5 with the backward, halved for
+    causal)."""
     from oracle import ref
-    import numpy as np
-    inp = W.make_inputs(w, shape=(1, min(w.H, 4), w.N, w.d))
-    q, k, v = (inp[n][0].to(__import__("torch").float64).numpy() for n in ("q", "k", "v"))
-    do = inp["do"][0].to(__import__("torch").float64).numpy() if "do" in inp else None
-    maskh = None if inp.get("mask") is None else inp["mask"][0, 0].to(__import__("torch").float64).numpy()
+    import torch
+    n = min(w.N, SAMPLE_ROWS)
+    if inp is None:
+        inp = W.make_inputs(w, shape=(1, min(w.H, 4), w.N, w.d))
+    nh = min(w.H, 4)
+    f64 = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    q, k, v = (f64(inp[x][0, :nh, :n]) for x in ("q", "k", "v"))
+    do = f64(inp["do"][0, :nh, :n]) if "do" in inp else None
+    maskh = None if inp.get("mask") is None else f64(inp["mask"][0, 0, :n, :n])
     t0 = time.perf_counter()
     heads = 0
     while True:
@@ -144,8 +163,14 @@ def oracle_sample(w: W.Workload, budget_s: float, max_heads=None):
         el = time.perf_counter() - t0
         if el >= budget_s or (max_heads and heads >= max_heads):
             break
-    flops = step_flops(W.Workload(**{**w.__dict__, "B": 1, "H": heads}))
-    return el, flops, heads
+    flops = step_flops(W.Workload(**{**w.__dict__, "B": 1, "H": heads, "N": n}))
+    return el, flops, heads, n
+
+
+def _sample_text(w, heads, n, el=None):
+    what = "whole head(s)" if n == w.N else f"leading {n} x {n} block(s) of head(s)"
+    t = f"{heads} {what} of the workload, fp64 oracle forward+backward"
+    return t + (f", {el:.1f} s" if el is not None else "")
 
 
 def host_cores() -> int:
@@ -158,23 +183,26 @@ def host_cores() -> int:
 def run_reference(args, w, rank, world):
     if rank != 0:
         return
+    inp = W.make_inputs(w)
     for _ in range(args.warmup):
-        oracle_sample(w, 0.0, max_heads=1)
-    secs, flops = [], []
+        oracle_sample(w, 0.0, max_heads=1, inp=inp)
+    secs, flops, heads, n = [], [], 0, w.N
     for _ in range(args.steps):
-        el, fl, _ = oracle_sample(w, args.ref_budget, max_heads=None)
+        el, fl, hd, n = oracle_sample(w, args.ref_budget, max_heads=None, inp=inp)
         secs.append(el)
         flops.append(fl)
+        heads += hd
     value = sum(flops) / sum(secs) / 1e12
     ms = 1000.0 * sum(secs) / len(secs)
+    sample = (f"per step, {_sample_text(w, '', n).strip()} until {args.ref_budget:.0f} s elapsed "
+              f"({heads} in {args.steps} steps)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {**w.describe(), "sample": "whole heads of the workload, fp64 oracle forward+backward, "
-                                            f"~{args.ref_budget:.0f} s per step"},
+        "config": {**w.describe(), "sample": sample},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-                         "sample": f"whole heads per step until {args.ref_budget:.0f} s elapsed"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -295,6 +323,7 @@ def run_ours(args, w, rank, world, local_rank):
         ws = torch.empty(max(A.bwd_workspace_size(q), 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do) if t is not None)
 
     def bwd():
         if w.backward:
@@ -372,7 +401,7 @@ def run_ours(args, w, rank, world, local_rank):
                                  "unit": "TFLOP/s", "frac": fwd_tflops / peak}}
     if w.backward:
         main_tflops = (f_step - f_fwd) / (ms_main * 1e-3) / 1e12
-        kernels["bwd_tc_kernel"] = {"ms": ms_main, "bound": "tensor", "achieved": main_tflops, "peak": peak,
+        kernels["bwd_tc64_kernel" if w.d == 64 else "bwd_tc_kernel"] = {"ms": ms_main, "bound": "tensor", "achieved": main_tflops, "peak": peak,
                                     "unit": "TFLOP/s", "frac": main_tflops / peak}
         rows = w.B * w.H * w.N
         pre_bytes = rows * w.d * 2 * 2 + rows * w.d * 4 + rows * 2 * 4 + rows * 4
@@ -460,7 +489,8 @@ def run_ours(args, w, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**w.describe(), "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "256 MiB buffer rewritten before every timed step (inputs fit in L2)",
+                   "l2": ("inputs larger than L2" if in_bytes > (129 << 20) else "inputs fit in L2") +
+                         "; a 256 MiB buffer is rewritten before every timed step",
                    "step": "attn_fwd + attn_bwd" if w.backward else "attn_fwd"},
         "pct_of_peak": 100.0 * value / world / peak,
         "fwd": {"ms": ms_fwd, "tflops": fwd_tflops, "pct_of_peak": 100.0 * fwd_tflops / peak},
@@ -492,10 +522,9 @@ def run_ours(args, w, rank, world, local_rank):
             table[f"decode_b8_h32_nq{nq}_nk8192_d128_bf16_causal"] = measure_decode(A, dev, peaks["hbm_gbs"], nq)
         line["workloads"] = table
     if world == 1 and not args.no_cpu_baseline:
-        el, fl, heads = oracle_sample(w, args.cpu_budget)
+        el, fl, heads, n = oracle_sample(w, args.cpu_budget, inp=inp)
         line["cpu_baseline"] = {"value": fl / el / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-                                "sample": f"{heads} whole head(s) of the workload, fp64 forward+backward, "
-                                          f"{el:.1f} s"}
+                                "sample": _sample_text(w, heads, n, el)}
     print(json.dumps(line), flush=True)
 
 
@@ -558,7 +587,7 @@ def run_table_entry(args):
     --warmup, L2 rewritten before each)."""
     import torch
     import attn_fwd_03_gb300 as A
-    every = {**W.WORKLOADS, **W.F16_WORKLOADS, **W.D256_WORKLOADS, **W.FP8_WORKLOADS}
+    every = {**W.WORKLOADS, **W.F16_WORKLOADS, **W.D256_WORKLOADS, **W.FP8_WORKLOADS, **W.PROFILE_WORKLOADS}
     by_name = {wk.name: wk for wk in every.values()}
     if args.table_workload not in by_name:
         raise SystemExit(f"unknown workload {args.table_workload}; one of {sorted(by_name)}")
@@ -578,7 +607,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", type=int, default=5, choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=5.0)

@@ -119,3 +119,35 @@ def test_clock_summary_skips_unreadable_rows():
     assert s["samples"] == 1 and s["sm_mhz"] == 2040.0
     empty = bench.ClockSampler(0)
     assert empty.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_oracle_sample_block_is_part_of_a_causal_workload():
+    # the CPU baseline times the leading n x n block of long heads; for causal attention the
+    # first n query rows see only the first n keys, so the block's O, LSE and dQ rows are the
+    # workload's own
+    import numpy as np
+    from oracle import ref
+    r = np.random.default_rng(5)
+    N, n, d = 300, 128, 16
+    q, k, v, do = (r.standard_normal((N, d)) for _ in range(4))
+    O, L = ref.forward_head(q, k, v, 0.25, True, rows=np.arange(n))
+    Ob, Lb = ref.forward_head(q[:n], k[:n], v[:n], 0.25, True)
+    assert np.allclose(O, Ob, rtol=0, atol=1e-13) and np.allclose(L, Lb, rtol=0, atol=1e-13)
+    dq = ref.backward_head(q, k, v, do, 0.25, True, q_rows=np.arange(n))[0]
+    dqb = ref.backward_head(q[:n], k[:n], v[:n], do[:n], 0.25, True)[0]
+    assert np.allclose(dq, dqb, rtol=0, atol=1e-12)
+
+
+def test_oracle_sample_counts_the_block_flops():
+    w = bench.W.WORKLOADS[5]
+    el, fl, heads, n = bench.oracle_sample(w, 0.0, max_heads=1, inp=_tiny_inputs(w))
+    assert n == bench.SAMPLE_ROWS and heads == 1
+    assert fl == 4 * n * n * w.d * 3.5 / 2
+
+
+def _tiny_inputs(w):
+    # the sampler reads only the leading block of each head: a tensor that long is enough
+    import torch
+    n = bench.SAMPLE_ROWS
+    return {x: torch.randn(1, 1, n, w.d, generator=torch.Generator().manual_seed(i)).to(torch.bfloat16)
+            for i, x in enumerate(("q", "k", "v", "do"))}
