@@ -147,10 +147,12 @@ __global__ void __launch_bounds__(384, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WaitCtl wc{p.err, &bar.abort_flag, p.timeout_ns};
 
-    // work unit: key tile kt of (b, h); early key tiles first (they see the most query tiles)
-    const int bh = p.B * p.H;
-    const int kt = blockIdx.x / bh;
-    const int b = (blockIdx.x % bh) / p.H, h = blockIdx.x % p.H;
+    // work unit: key tile kt of (b, h). Heads outermost, so the CTAs resident at any time
+    // work on one or two heads and their dQ reductions and Q / dO reads stay in L2; within a
+    // head early key tiles first (under causal masking they see the most query tiles).
+    const int kt = blockIdx.x % p.n_ktiles;
+    const int bh_i = blockIdx.x / p.n_ktiles;
+    const int b = bh_i / p.H, h = bh_i % p.H;
     const int k0 = kt * BK;
     const int nq_all = (p.N + BQ - 1) / BQ;
     const int i_begin = p.causal ? kt : 0;  // first query tile on or below the diagonal

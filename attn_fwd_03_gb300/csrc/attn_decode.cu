@@ -7,11 +7,13 @@
 // work unit therefore takes one (b, h) and one contiguous key range (a
 // split), runs the online softmax of "Explain FlashAttention and why it is
 // IO-aware" over that range for every query row, and writes the row's
-// partial state: the running max m, the sum l of 2^(s - m) and the
-// unnormalised o. The per-split pass runs on the tensor cores
-// (attn_decode_tc.cu). The combine kernel here merges the splits of a row
-// with the same rescaling that merges tiles:
-//   M = max m_s, L = sum l_s 2^(m_s - M), O = sum o_s 2^(m_s - M) / L.
+// partial state: the running max m, the sum l of 2^(s - m), the divisor lo
+// of o (l with its largest term as rounded for the P V product: see
+// o_divisor in ptx.cuh) and the unnormalised o. The per-split pass runs on
+// the tensor cores (attn_decode_tc.cu). The combine kernel here merges the
+// splits of a row with the same rescaling that merges tiles:
+//   M = max m_s, w_s = 2^(m_s - M), O = sum w_s o_s / sum w_s lo_s,
+//   LSE = ln 2 (M + log2 sum w_s l_s).
 // Scores are in the log2 domain: s = c * (q . k) with c = scale * log2(e).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -35,7 +37,7 @@ struct CombineArgs {
     long long o_sb, o_sh, o_sn;  // elements
     int B, H, nq;
     int splits;    // key ranges per (b, h)
-    float* part;   // [B*H][splits][nq][D + 4]: m, l, 2 unused, o[D]
+    float* part;   // [B*H][splits][nq][D + 4]: m, l, lo, 1 unused, o[D]
 };
 
 template <int D>
@@ -58,7 +60,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(CombineArgs a) {
     for (int s = lane; s < a.splits; s += 32) M = fmaxf(M, base[s * sstride]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    float L = 0.f, out[PER];
+    float L = 0.f, Lo = 0.f, out[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) out[e] = 0.f;
     if (M != -INFINITY) {
@@ -66,11 +68,12 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(CombineArgs a) {
             const float* r = base + s * sstride;
             const float w = ptx::ex2(r[0] - M);  // 0 for a split that saw no key of this row
             L += w * r[1];
+            Lo += w * r[2];
 #pragma unroll
             for (int e = 0; e < PER; ++e) out[e] = fmaf(w, r[4 + lane * PER + e], out[e]);
         }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const float inv = Lo > 0.f ? 1.f / Lo : 0.f;
     uint16_t* orow = reinterpret_cast<uint16_t*>(a.o) + (b * a.o_sb + h * a.o_sh + (long long)i * a.o_sn);
     if constexpr (PER == 2) {
         *reinterpret_cast<uint32_t*>(orow + lane * 2) = ptx::pack_h16<F16>(out[0] * inv, out[1] * inv);

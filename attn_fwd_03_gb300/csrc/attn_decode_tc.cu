@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const DtcUnit w = dtc_unit(p, u);
             // keys this row may see: [key0, lim)
             const int lim = p.causal ? min(w.key_end, p.nk - p.nq + r + 1) : w.key_end;
-            float m_ref = -INFINITY, l = 0.f;
+            float m_ref = -INFINITY, m_row = -INFINITY, l = 0.f;
             for (int j = 0; j < w.ntiles; ++j) {
                 ok = mbar_wait(&bar.s_full, scnt & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
@@ -311,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mx[c] = m;
                 }
                 const float m_tile = fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], mx[4]), fmax3(mx[5], mx[6], mx[7]));
+                m_row = fmaxf(m_row, m_tile);
                 float m_new = m_ref;
                 if (m_tile > m_ref + kRescaleThreshold) m_new = m_tile;
                 const bool moved = m_new != m_ref;
@@ -371,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r < p.nq) {
                 rec[0] = l > 0.f ? m_ref : -INFINITY;
                 rec[1] = l;
+                rec[2] = o_divisor<F16>(l, m_row, m_ref);  // divisor of o (see o_divisor)
             }
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {

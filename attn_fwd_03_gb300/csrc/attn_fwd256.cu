@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ku = 0, u = unit_at(0); u < p.num_units && ok; u = unit_at(++ku)) {
             const F256Unit w = f256_unit(p, u);
             const int row = w.qt * BM + r;
-            float m_ref = -INFINITY, l = 0.f;
+            float m_ref = -INFINITY, m_row = -INFINITY, l = 0.f;
             for (int j = 0; j < w.nkv; ++j) {
                 ok = mbar_wait(&bar.s_full, scnt & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
@@ -461,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float m_tile =
                     fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], mx[4]), fmax3(mx[5], mx[6], mx[7])) * cc;
+                m_row = fmaxf(m_row, m_tile);
                 float m_new = m_ref;
                 if (m_tile > m_ref + kRescaleThreshold) m_new = m_tile;
                 const bool moved = m_new != m_ref;
@@ -535,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ++pvcnt;
             tc_fence_after();
-            const float inv = l > 0.f ? p.o_factor / l : 0.f;
+            const float den = E::kF8 ? o_divisor_e4m3(l, m_row, m_ref) : o_divisor<F16>(l, m_row, m_ref);
+            const float inv = den > 0.f ? p.o_factor / den : 0.f;
             __nv_bfloat16* orow = p.o + w.b * p.o_sb + w.h * p.o_sh + (long long)row * p.o_sn;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {

@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
             const int nkv = w.nkv[t];
             if (nkv == 0) continue;
             const int row = w.row0[t] + r;
-            float m_ref = -INFINITY, l = 0.f;
+            float m_ref = -INFINITY, m_row = -INFINITY, l = 0.f;
             for (int j = 0; j < nkv; ++j) {
                 ok = mbar_wait(&bar.s_full[t], scnt & 1, wc);
                 ok = __all_sync(0xffffffffu, ok);
@@ -562,6 +562,7 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                 }
                 const float m_tile =
                     fmaxf(fmax3(fmax3(mx[0], mx[1], mx[2]), mx[3], mx[4]), fmax3(mx[5], mx[6], mx[7])) * cc;
+                m_row = fmaxf(m_row, m_tile);
                 float m_new = m_ref;
                 if (m_tile > m_ref + kRescaleThreshold) m_new = m_tile;
                 const bool moved = m_new != m_ref;
@@ -653,7 +654,8 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                 ++ocnt;
             }
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float den = o_divisor<F16>(l, m_row, m_ref);
+            const float inv = den > 0.f ? 1.f / den : 0.f;
             __nv_bfloat16* orow = p.o + w.b * p.o_sb + w.h * p.o_sh + (long long)row * p.o_sn;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {

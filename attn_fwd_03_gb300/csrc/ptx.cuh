@@ -386,6 +386,19 @@ __device__ __forceinline__ float2 unpack_h16(uint32_t v) {
         return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
     }
 }
+// Divisor of O in the online softmax with a lagging reference max m_ref. l sums the unrounded
+// p_j = 2^(s_j - m_ref); the P V product used them rounded to the 16-bit operand type. The
+// row's largest p, 2^(m_row - m_ref) >= 1 (m_row: the row's running max), is generally not a
+// 16-bit number, and dividing by the unrounded l would carry its rounding into the whole row of
+// O. Swapping that one term of l for its rounded value makes the largest weight cancel as in the
+// product. (0 when l is 0: a row with nothing to attend to.)
+template <bool F16>
+__device__ __forceinline__ float o_divisor(float l, float m_row, float m_ref) {
+    if (!(l > 0.f)) return 0.f;
+    const float pm = ex2(m_row - m_ref);
+    return l + (unpack_h16<F16>(pack_h16<F16>(pm, pm)).x - pm);
+}
+
 template <bool F16>
 __device__ __forceinline__ float h16_to_float(uint16_t v) {
     if constexpr (F16)

@@ -45,5 +45,21 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, fl
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// E4M3 rounding of x (0 <= x <= 448) as a float.
+__device__ __forceinline__ float round_e4m3(float x) {
+    uint16_t c;
+    uint32_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(c) : "f"(x));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(c));
+    return ptx::unpack_h16<true>(h).x;
+}
+
+// ptx::o_divisor for P rounded to E4M3.
+__device__ __forceinline__ float o_divisor_e4m3(float l, float m_row, float m_ref) {
+    if (!(l > 0.f)) return 0.f;
+    const float pm = ptx::ex2(m_row - m_ref);
+    return l + (round_e4m3(pm) - pm);
+}
+
 }  // namespace ptx_f8
 }  // namespace attn

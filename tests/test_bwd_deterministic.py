@@ -150,22 +150,34 @@ def test_empty_problem(A):
 
 
 @pytest.mark.parametrize("idx", [2, 4, 5])
-def test_full_size_sampled(A, idx):
+def test_full_size_whole_head(A, idx):
+    """Full size, one whole head element by element: the head's saved O and LSE from the
+    oracle, then chained on the kernel forward's own (see the attn_bwd test of the same name)."""
     w = W.WORKLOADS[idx]
     inp = W.make_inputs(w)
-    dq, dk, dv = _run(A, inp, w.causal, w.scale, saved="kernel")
+    q, k, v, mask, do = (_dev(inp.get(n)) for n in ("q", "k", "v", "mask", "do"))
+    o, lse = A.attn_fwd(q, k, v, scale=w.scale, causal=w.causal, mask=mask)
     b, h = w.B - 1, w.H // 2
-    r = np.random.default_rng(300 + idx)
-    rows = np.array(sorted(set(r.choice(w.N, size=48, replace=False).tolist()) | {0, w.N - 1, 127, 128}))
     maskh = None if inp.get("mask") is None else to64(inp["mask"][b, 0])
     hargs = (to64(inp["q"][b, h]), to64(inp["k"][b, h]), to64(inp["v"][b, h]), to64(inp["do"][b, h]), w.scale,
              w.causal, maskh)
-    pure = ref.backward_head(*hargs, q_rows=rows, k_rows=rows)
-    stored = ref.backward_head(*hargs, q_rows=rows, k_rows=rows, o_storage="bf16")
-    for i, (name, g) in enumerate((("dQ", dq), ("dK", dk), ("dV", dv))):
-        assert_grad(name, g[b, h, rows], stored[i], pure[i])
-    for t in (dq, dk, dv):
+    stored = ref.backward_head(*hargs, o_storage="bf16")
+    pure = ref.backward_head(*hargs)
+    chained = A.attn_bwd_deterministic(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask)
+    chained = [g[b, h].cpu() for g in chained]
+    O, L = ref.forward_head(*hargs[:3], w.scale, w.causal, maskh)
+    o[b, h] = torch.from_numpy(ref.round_bf16(O)).to(o.dtype).to(o.device)
+    lse[b, h] = torch.from_numpy(L).to(torch.float32).to(lse.device)
+    fed = A.attn_bwd_deterministic(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, mask=mask)
+    torch.cuda.synchronize()
+    assert A.attn_status() == A.ATTN_OK, A.last_error()
+    for t in fed:
         assert torch.isfinite(t).all()
+    for label, grads in (("oracle-saved O, LSE", [g[b, h] for g in fed]), ("chained", chained)):
+        for i, (name, g) in enumerate(zip(("dQ", "dK", "dV"), grads)):
+            e = assert_grad(f"{label} {name}", g, stored[i], pure[i])
+            print(f"[{w.name} b={b} h={h}] deterministic {label} {name}: stored max-abs {e['stored'][0]:.3e} "
+                  f"rel-L2 {e['stored'][1]:.3e}; pure max-abs {e['pure'][0]:.3e} rel-L2 {e['pure'][1]:.3e}")
 
 
 def test_bnhd_strided_layout(A):

@@ -8,10 +8,15 @@ rounded to E4M3 before it multiplies V. With p_j = exp(s_j - m) <= 1 for the
 row max m, the kernel holds p_j 2^k for some 0 <= k <= 8 (its reference max
 sits up to 8 below m in log2 units), so the rounding error of p_j is at most
 2^-4 p_j when p_j 2^k is a normal E4M3 value (>= 2^-6) and at most
-2^-10 2^-k <= 2^-10 otherwise; l sums the unrounded values. Hence per element
-    |O_kernel - O| <= sum_j e_j |v_jd| / l,   e_j = max(2^-4 p_j, 2^-10 [0 < p_j < 2^-6])
+2^-10 2^-k <= 2^-10 otherwise. O is divided by l, the sum of the unrounded
+values, with its largest term p_* swapped for the rounded one: l~ = l + eps_*
+(eps_j = p~_j - p_j; the common factor 2^k cancels). Then
+    O_kernel - O = (sum_j eps_j v_j - eps_* O) / l~,
+so per element, whichever largest term the kernel picked,
+    |O_kernel - O| <= (sum_j e_j |v_jd| + e_max |O_d|) / (l - e_max),
+    e_j = max(2^-4 p_j, 2^-10 [0 < p_j < 2^-6]),  e_max = max_j e_j,
 plus the bf16 rounding of the output (2^-8 relative, with slack for fp32).
-LSE is unaffected by the rounding of P and keeps the 1e-3 bound.
+LSE comes from the unrounded l and keeps the 1e-3 bound.
 """
 import math
 
@@ -58,7 +63,9 @@ def _bound_and_ref(inp, scale, causal, mask, heads=None, rows=None):
         p = np.where(empty, 0.0, np.exp(s - np.where(empty, 0.0, m)))
         lsum = p.sum(axis=1, keepdims=True)
         e = np.maximum(2.0 ** -4 * p, np.where((p > 0) & (p < 2.0 ** -6), 2.0 ** -10, 0.0))
-        bound = (e @ np.abs(v)) / np.where(lsum > 0, lsum, 1.0)
+        emax = e.max(axis=1, keepdims=True) if e.shape[1] else np.zeros_like(lsum)
+        low = lsum - emax
+        bound = (e @ np.abs(v) + emax * np.abs(O)) / np.where(low > 0, low, 1.0)
         res[(b, h)] = (O, L, bound)
     return res
 
