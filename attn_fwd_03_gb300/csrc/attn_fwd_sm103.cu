@@ -99,7 +99,8 @@ struct FwdCfg {
 struct FwdParamsDev {
     int B, H, N;
     int causal;
-    float c;  // scale * log2(e)
+    float c;          // scale * log2(e)
+    float inv_scale;  // 1 / scale: the additive mask in units of the raw scores
     float* lse;
     __nv_bfloat16* o;
     long long o_sb, o_sh, o_sn;
@@ -510,44 +511,41 @@ __global__ void __launch_bounds__(FwdCfg<D, MASK>::kThreads, 1)
                 }
                 const bool diag = p.causal && (j == nkv - 1);
                 const bool tail = (j + 1) * BN > p.N;
-                float cc = p.c;
-                if (MASK || diag || tail) {
-                    // generic path: fold scale, mask, causal and tail into s (log2 domain)
+                // s stays in raw score units (times cc = scale * log2(e) below); the additive
+                // mask enters as mask / scale, one packed FMA per pair of columns
+                const float cc = p.c;
+                if (MASK) {
+                    ok = mbar_wait(&bar.m_full[t], mcnt & 1, wc);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    ++mcnt;
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx) {
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const uint4 mv = *reinterpret_cast<const uint4*>(
+                                mtile + bx * BM * 128 + r * 128 + ((ch ^ (r & 7)) << 4));
+                            const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int col = bx * 64 + ch * 8 + 2 * e;
+                                const float2 x = ffma2(unpack_h16<F16>(mw[e]), make_float2(p.inv_scale, p.inv_scale),
+                                                       make_float2(__uint_as_float(su[col]), __uint_as_float(su[col + 1])));
+                                su[col] = __float_as_uint(x.x);
+                                su[col + 1] = __float_as_uint(x.y);
+                            }
+                        }
+                    }
+                    mbar_arrive(&bar.m_empty[t]);
+                }
+                if (diag || tail) {  // causal on absolute positions, and the key tail
                     const int key0 = j * BN;
                     const int lim_causal = diag ? row - key0 : BN;  // keys with index <= row survive
                     const int lim_tail = p.N - key0;
                     const int lim = min(lim_causal + 1, lim_tail);  // first masked column
-                    if (MASK) {
-                        ok = mbar_wait(&bar.m_full[t], mcnt & 1, wc);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) break;
-                        ++mcnt;
-#pragma unroll
-                        for (int bx = 0; bx < 2; ++bx) {
-#pragma unroll
-                            for (int ch = 0; ch < 8; ++ch) {
-                                const uint4 mv = *reinterpret_cast<const uint4*>(
-                                    mtile + bx * BM * 128 + r * 128 + ((ch ^ (r & 7)) << 4));
-                                const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 f = unpack_h16<F16>(mw[e]);
-                                    const int col = bx * 64 + ch * 8 + 2 * e;
-                                    su[col] = __float_as_uint(fmaf(__uint_as_float(su[col]), p.c, f.x * kLog2e));
-                                    su[col + 1] =
-                                        __float_as_uint(fmaf(__uint_as_float(su[col + 1]), p.c, f.y * kLog2e));
-                                }
-                            }
-                        }
-                        mbar_arrive(&bar.m_empty[t]);
-                    } else {
-#pragma unroll
-                        for (int col = 0; col < BN; ++col) su[col] = __float_as_uint(__uint_as_float(su[col]) * p.c);
-                    }
 #pragma unroll
                     for (int col = 0; col < BN; ++col)
                         if (col >= lim) su[col] = __float_as_uint(-INFINITY);
-                    cc = 1.f;
                 }
                 // tile max (in the log2 domain after multiplying by cc): 3-input max, eight
                 // independent chains of 16 columns each
@@ -702,6 +700,7 @@ cudaError_t launch_tc(const attn_fwd_params& prm, const FwdMaps& maps, const Lau
     p.N = prm.N;
     p.causal = prm.causal;
     p.c = prm.scale * kLog2e;
+    p.inv_scale = 1.f / prm.scale;
     p.lse = prm.lse;
     p.o = static_cast<__nv_bfloat16*>(prm.o);
     p.o_sb = prm.o_stride[0];
