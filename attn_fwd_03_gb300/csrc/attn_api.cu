@@ -318,6 +318,45 @@ attn_status_t build_bwd_maps(const attn_bwd_params& p, BwdMaps* m) {
     return encode_h16_map(&m->dout, "dout", p.dout, d, N, p.fwd.H, p.fwd.B, p.do_stride, 128, DT);
 }
 
+attn_status_t build_bwd256_maps(const attn_bwd_params& p, Bwd256Maps* m) {
+    FwdMaps f;
+    attn_status_t st = build_fwd_maps(p.fwd, &f);
+    if (st != ATTN_OK) return st;
+    m->k = f.k;
+    m->v = f.v;
+    const uint64_t N = (uint64_t)p.fwd.N, d = (uint64_t)p.fwd.d;
+    const int32_t DT = p.fwd.dtype;
+    if ((st = encode_h16_map(&m->q64, "q", p.fwd.q, d, N, p.fwd.H, p.fwd.B, p.fwd.q_stride, 64, DT)) != ATTN_OK)
+        return st;
+    if ((st = encode_h16_map(&m->do64, "dout", p.dout, d, N, p.fwd.H, p.fwd.B, p.do_stride, 64, DT)) != ATTN_OK)
+        return st;
+    if (p.fwd.mask) {
+        const uint64_t hm = p.fwd.mask_stride[1] != 0 ? (uint64_t)p.fwd.H : 1;
+        const uint64_t bm = p.fwd.mask_stride[0] != 0 ? (uint64_t)p.fwd.B : 1;
+        return encode_h16_map(&m->mask64, "mask", p.fwd.mask, N, N, hm, bm, p.fwd.mask_stride, 64, DT);
+    }
+    m->mask64 = m->q64;  // unused by the kernel variant without a mask
+    return ATTN_OK;
+}
+
+// The recompute kernel of a backward pass: head dim 256 has its own kernel and maps.
+attn_status_t launch_bwd_main(const attn_bwd_params& p, const BwdWorkspace& ws, const LaunchCommon& lc,
+                              cudaStream_t s) {
+    attn_status_t st;
+    cudaError_t e;
+    if (p.fwd.d == 256) {
+        Bwd256Maps maps;
+        if ((st = build_bwd256_maps(p, &maps)) != ATTN_OK) return st;
+        e = launch_bwd256(p, maps, ws, lc, s);
+    } else {
+        BwdMaps maps;
+        if ((st = build_bwd_maps(p, &maps)) != ATTN_OK) return st;
+        if ((st = encode_dq_acc_map(p.fwd, ws.dq_acc, &maps.dq_acc)) != ATTN_OK) return st;
+        e = launch_bwd_tc(p, maps, ws, lc, s);
+    }
+    return e != cudaSuccess ? cuda_fail(e, "backward main launch") : ATTN_OK;
+}
+
 }  // namespace
 
 static size_t stats_bytes(const attn_fwd_params& p) {
@@ -355,7 +394,6 @@ attn_status_t bwd_check_inputs(const attn_bwd_params* p, bool* empty) {
     attn_status_t st = check_fwd(&p->fwd, empty);
     if (st != ATTN_OK) return st;
     if (p->fwd.dtype == ATTN_F32) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for bf16 and fp16 only");
-    if (p->fwd.d == 256) return fail(ATTN_ERR_UNSUPPORTED, "backward is built for head dim 64 and 128");
     if (*empty) return ATTN_OK;
     if ((st = check_tensor("dout", p->dout, p->do_stride, 2, false)) != ATTN_OK) return st;
     if ((st = check_tensor("dq", p->dq, p->dq_stride, 2, false)) != ATTN_OK) return st;
@@ -377,12 +415,9 @@ attn_status_t bwd_launch_with(const attn_bwd_params& p, const BwdWorkspace& ws, 
     attn_status_t st = device_setup(&lc);
     if (st != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    BwdMaps maps;
-    if ((st = build_bwd_maps(p, &maps)) != ATTN_OK) return st;
-    if ((st = encode_dq_acc_map(p.fwd, ws.dq_acc, &maps.dq_acc)) != ATTN_OK) return st;
     cudaError_t e = launch_bwd_prepass(p, ws, lc.err, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward pre-pass launch");
-    if ((e = launch_bwd_tc(p, maps, ws, lc, s)) != cudaSuccess) return cuda_fail(e, "backward main launch");
+    if ((st = launch_bwd_main(p, ws, lc, s)) != ATTN_OK) return st;
     if ((e = launch_bwd_dq_finalize(p, ws, lc.err, s)) != cudaSuccess)
         return cuda_fail(e, "backward dQ finalize launch");
     return ATTN_OK;
@@ -428,7 +463,7 @@ attn_status_t attn_fwd_fp8(const attn_fwd_fp8_params* p, void* stream) {
 }
 
 size_t attn_bwd_workspace_size(const attn_fwd_params* p) {
-    if (!p || p->B < 0 || p->H < 0 || p->N < 0 || (p->d != 64 && p->d != 128)) return 0;
+    if (!p || p->B < 0 || p->H < 0 || p->N < 0 || (p->d != 64 && p->d != 128 && p->d != 256)) return 0;
     return bwd_workspace_bytes(*p);
 }
 
@@ -445,14 +480,11 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
     if ((st = device_setup(&lc)) != ATTN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const BwdWorkspace ws = bwd_workspace_split(*p);
-    BwdMaps maps;
-    if ((st = build_bwd_maps(*p, &maps)) != ATTN_OK) return st;
-    if ((st = encode_dq_acc_map(p->fwd, ws.dq_acc, &maps.dq_acc)) != ATTN_OK) return st;
     cudaError_t e = record_bwd_event(0, s);
     if (e == cudaSuccess) e = launch_bwd_prepass(*p, ws, lc.err, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd pre-pass launch");
-    if ((e = record_bwd_event(1, s)) == cudaSuccess) e = launch_bwd_tc(*p, maps, ws, lc, s);
-    if (e != cudaSuccess) return cuda_fail(e, "attn_bwd main launch");
+    if ((e = record_bwd_event(1, s)) != cudaSuccess) return cuda_fail(e, "attn_bwd event record");
+    if ((st = launch_bwd_main(*p, ws, lc, s)) != ATTN_OK) return st;
     if ((e = record_bwd_event(2, s)) == cudaSuccess) e = launch_bwd_dq_finalize(*p, ws, lc.err, s);
     if (e != cudaSuccess) return cuda_fail(e, "attn_bwd dQ finalize launch");
     if ((e = record_bwd_event(3, s)) != cudaSuccess) return cuda_fail(e, "attn_bwd event record");
@@ -460,6 +492,8 @@ attn_status_t attn_bwd(const attn_bwd_params* p, void* stream) {
 }
 
 attn_status_t attn_bwd_deterministic(const attn_bwd_params* p, void* stream) {
+    if (p && p->fwd.d == 256)
+        return fail(ATTN_ERR_UNSUPPORTED, "the deterministic backward is built for head dim 64 and 128");
     bool empty = false;
     attn_status_t st = bwd_check_inputs(p, &empty);
     if (st != ATTN_OK || empty) return st;

@@ -361,9 +361,13 @@ cudaError_t launch_bwd_prepass(const attn_bwd_params& p, const BwdWorkspace& ws,
     const SimtArgs a = make_bwd_args(p, ws);
     const RowGrid g = row_grid((long long)p.fwd.B * p.fwd.H * ((p.fwd.N + 127) / 128 * 128), p.fwd.d);
     const bool f16 = p.fwd.dtype == ATTN_F16;
-    const cudaError_t e = p.fwd.d == 64
-                              ? (f16 ? prepass_t<64, true>(g, a, ws, err, s) : prepass_t<64, false>(g, a, ws, err, s))
-                              : (f16 ? prepass_t<128, true>(g, a, ws, err, s) : prepass_t<128, false>(g, a, ws, err, s));
+    cudaError_t e;
+    if (p.fwd.d == 64)
+        e = f16 ? prepass_t<64, true>(g, a, ws, err, s) : prepass_t<64, false>(g, a, ws, err, s);
+    else if (p.fwd.d == 128)
+        e = f16 ? prepass_t<128, true>(g, a, ws, err, s) : prepass_t<128, false>(g, a, ws, err, s);
+    else
+        e = f16 ? prepass_t<256, true>(g, a, ws, err, s) : prepass_t<256, false>(g, a, ws, err, s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -371,9 +375,13 @@ cudaError_t launch_bwd_dq_finalize(const attn_bwd_params& p, const BwdWorkspace&
     const SimtArgs a = make_bwd_args(p, ws);
     const RowGrid g = row_grid((long long)p.fwd.B * p.fwd.H * p.fwd.N, p.fwd.d);
     const bool f16 = p.fwd.dtype == ATTN_F16;
-    const cudaError_t e =
-        p.fwd.d == 64 ? (f16 ? finalize_t<64, true>(g, a, ws, err, s) : finalize_t<64, false>(g, a, ws, err, s))
-                      : (f16 ? finalize_t<128, true>(g, a, ws, err, s) : finalize_t<128, false>(g, a, ws, err, s));
+    cudaError_t e;
+    if (p.fwd.d == 64)
+        e = f16 ? finalize_t<64, true>(g, a, ws, err, s) : finalize_t<64, false>(g, a, ws, err, s);
+    else if (p.fwd.d == 128)
+        e = f16 ? finalize_t<128, true>(g, a, ws, err, s) : finalize_t<128, false>(g, a, ws, err, s);
+    else
+        e = f16 ? finalize_t<256, true>(g, a, ws, err, s) : finalize_t<256, false>(g, a, ws, err, s);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

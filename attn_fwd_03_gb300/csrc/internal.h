@@ -62,6 +62,12 @@ struct BwdMaps {
     CUtensorMap dk, dv;  // outputs (64 x 128 boxes, 128-byte swizzle) for TMA stores of dK / dV tiles
 };
 
+// Tensor maps for the head-dim-256 backward: K, V with 128-row boxes; Q, dO and the mask with
+// 64-row boxes (64-query tiles).
+struct Bwd256Maps {
+    CUtensorMap q64, k, v, do64, mask64;
+};
+
 // The two parts of the backward workspace.
 //  stats:  per (b, h) and 128-row query tile, 128 values of -LSE * log2(e)
 //          (-inf for fully masked rows and padding rows) followed by 128 values
@@ -119,6 +125,10 @@ cudaError_t launch_fwd256(const attn_fwd_params& p, const FwdMaps& maps, const L
 
 // attn_bwd_sm103.cu — tcgen05 backward main kernel (bf16).
 cudaError_t launch_bwd_tc(const attn_bwd_params& p, const BwdMaps& maps, const BwdWorkspace& ws,
+                          const LaunchCommon& lc, cudaStream_t s);
+
+// attn_bwd256.cu — tcgen05 backward at head dim 256 (one half of the head dim of dK, dV, dQ per CTA).
+cudaError_t launch_bwd256(const attn_bwd_params& p, const Bwd256Maps& maps, const BwdWorkspace& ws,
                           const LaunchCommon& lc, cudaStream_t s);
 
 // attn_bwd_dq.cu — query-stationary tcgen05 dQ kernel (fixed order of additions); writes dQ

@@ -142,8 +142,9 @@ def test_bwd_argument_errors(binding, entry):
     bp = binding.BwdParams()
     bp.fwd = _params(binding, dtype=binding.ATTN_F32)
     assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_UNSUPPORTED
-    bp.fwd = _params(binding, d=256)  # the forward only, so far
-    assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_UNSUPPORTED
+    bp.fwd = _params(binding, d=256)  # built for attn_bwd; the deterministic backward stops at 128
+    want = binding.ATTN_ERR_UNSUPPORTED if entry == "attn_bwd_deterministic" else binding.ATTN_ERR_INVALID
+    assert call(ctypes.byref(bp), None) == want
     bp.fwd = _params(binding)
     assert call(ctypes.byref(bp), None) == binding.ATTN_ERR_INVALID  # dout NULL
     fake = 1 << 20
@@ -158,9 +159,10 @@ def test_bwd_argument_errors(binding, entry):
 def test_workspace_size(binding):
     # per (b, h) and 128-row tile: 2 x 128 fp32 statistics; then the fp32 dQ accumulator
     for N in (100, 128, 300):
-        p = _params(binding, B=2, H=3, N=N, d=128)
-        tiles = 2 * 3 * ((N + 127) // 128)
-        assert binding.lib.attn_bwd_workspace_size(ctypes.byref(p)) == tiles * 1024 + 2 * 3 * N * 128 * 4
+        for d in (64, 128, 256):
+            p = _params(binding, B=2, H=3, N=N, d=d)
+            tiles = 2 * 3 * ((N + 127) // 128)
+            assert binding.lib.attn_bwd_workspace_size(ctypes.byref(p)) == tiles * 1024 + 2 * 3 * N * d * 4
 
 
 def test_version_and_timeout_knobs(binding):

@@ -86,11 +86,11 @@ WORKLOADS: Dict[int, Workload] = {
 F16_WORKLOADS[6] = dataclasses.replace(WORKLOADS[2], index=6, name="b4_h16_n2048_d64_f16_causal_fwd_bwd", dtype="f16")
 
 # Head dim 256 (FlashAttention-2 covers head dims up to 256: "What is FlashAttention?",
-# "Trade-offs and edge cases"), forward only: the 8,192-token layer shape with half the heads, so the
-# FLOPs equal the d = 128 layer's.
+# "Trade-offs and edge cases"), forward and backward: the 8,192-token layer shape with half the
+# heads, so the FLOPs equal the d = 128 layer's.
 D256_WORKLOADS: Dict[int, Workload] = {
-    7: Workload(7, "b1_h16_n8192_d256_bf16_fwd", 1, 16, 8192, 256, "bf16", False, False, False),
-    8: Workload(8, "b1_h16_n8192_d256_bf16_causal_fwd", 1, 16, 8192, 256, "bf16", True, False, False),
+    7: Workload(7, "b1_h16_n8192_d256_bf16_fwd_bwd", 1, 16, 8192, 256, "bf16", False, False, True),
+    8: Workload(8, "b1_h16_n8192_d256_bf16_causal_fwd_bwd", 1, 16, 8192, 256, "bf16", True, False, True),
 }
 
 
