@@ -84,7 +84,7 @@ typedef enum attn_dtype_t {
  */
 typedef struct attn_fwd_params {
     int32_t B, H, N, d;      /* batch, heads, sequence length, head dim: 64 or 128;
-                                256 for the bf16 / fp16 forward only */
+                                256 for bf16 / fp16 (forward and attn_bwd) */
     int32_t dtype;           /* attn_dtype_t of Q, K, V, O (and the mask) */
     int32_t causal;          /* 1: key j is masked for query i iff j > i (absolute
                                 positions, 0-based; same N for queries and keys) */
@@ -107,7 +107,12 @@ typedef struct attn_fwd_params {
  * Backward problem: dQ, dK, dV of sum(dO * O) for the forward described by
  * `fwd`, whose o and lse (as written by attn_fwd) are READ here. Recomputes
  * S and P tile by tile; no gradient flows to the mask. bf16 and fp16 at
- * head dim 64 or 128 (ATTN_F32 and head dim 256 return ATTN_ERR_UNSUPPORTED).
+ * head dim 64, 128 or 256 (ATTN_F32 returns ATTN_ERR_UNSUPPORTED). At head
+ * dim 256 the fp32 dK and dV of one key tile would fill tensor memory, so
+ * each key tile is handled by two CTAs, one per half of the head dimension,
+ * each recomputing the scores over the whole head dimension: 7/5 of the
+ * minimal tensor-core work. ("What is FlashAttention?", "Trade-offs and edge
+ * cases": FlashAttention-2 covers head dims up to 256.)
  */
 typedef struct attn_bwd_params {
     attn_fwd_params fwd;
@@ -157,7 +162,8 @@ ATTN_API attn_status_t attn_fwd_fp8(const attn_fwd_fp8_params *p, void *stream);
  * fp32 dQ accumulator [B, H, N, d]. */
 ATTN_API size_t attn_bwd_workspace_size(const attn_fwd_params *p);
 
-/* Backward pass: D pre-pass, recompute-and-accumulate kernel, dQ finalize. */
+/* Backward pass: D pre-pass, recompute-and-accumulate kernel, dQ finalize.
+ * Head dims 64, 128 and 256 (see attn_bwd_params). */
 ATTN_API attn_status_t attn_bwd(const attn_bwd_params *p, void *stream);
 
 /* The same backward pass without a caller workspace: the scratch (row
@@ -194,7 +200,8 @@ ATTN_API attn_status_t attn_bwd_noalloc(const attn_bwd_params *p, void *stream);
  * in order ("What is FlashAttention?", Step 3 loop order, Step 4 recompute)
  * and writes dQ once; dK and dV come from attn_bwd's key-stationary kernel,
  * whose sums over query tiles already run in a fixed order.
- *  - Arguments, workspace and errors exactly as attn_bwd.
+ *  - Arguments, workspace and errors exactly as attn_bwd, except that head
+ *    dim 256 returns ATTN_ERR_UNSUPPORTED (built for 64 and 128).
  *  - It does about 1.4 times the tensor-core work of attn_bwd (the scores
  *    and dP are computed twice). Results agree with attn_bwd's to rounding. */
 ATTN_API attn_status_t attn_bwd_deterministic(const attn_bwd_params *p, void *stream);
