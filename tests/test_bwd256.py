@@ -109,6 +109,20 @@ def test_strided_layout(A):
         assert_grad(name, g, stored[i])
 
 
+def test_dk_dv_identical_across_calls(A):
+    """dK and dV of a key tile are summed in one CTA in a fixed order, so repeated calls give the
+    same bits (dQ's reductions from different CTAs may land in any order)."""
+    inp = {n: t.cuda() for n, t in _inputs((1, 3, 700, 256), 5700).items()}
+    o, lse = A.attn_fwd(inp["q"], inp["k"], inp["v"], causal=True)
+    first = A.attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], causal=True)
+    for _ in range(3):
+        again = A.attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], causal=True)
+        torch.cuda.synchronize()
+        assert A.attn_status() == A.ATTN_OK, A.last_error()
+        assert torch.equal(first[1], again[1]) and torch.equal(first[2], again[2])
+        assert (first[0] - again[0]).abs().max().item() <= 1e-2 * max(1.0, first[0].abs().max().item())
+
+
 def test_deterministic_entry_rejects_head_dim_256(A):
     inp = {n: t.cuda() for n, t in _inputs((1, 1, 128, 256), 5600).items()}
     o, lse = A.attn_fwd(inp["q"], inp["k"], inp["v"])

@@ -94,15 +94,6 @@ def test_poisoned_outputs_fully_written(A):
     assert not torch.isnan(o).any() and not torch.isnan(lse).any()
 
 
-def test_backward_is_not_built(A):
-    inp = _inputs((1, 1, 128, 256), 3700)
-    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o, lse = A.attn_fwd(q, k, v)
-    with pytest.raises(A.AttnError) as ei:
-        A.attn_bwd(q, k, v, o, lse, q)
-    assert ei.value.status == A.ATTN_ERR_UNSUPPORTED
-
-
 @pytest.mark.parametrize("idx", sorted(W.D256_WORKLOADS))
 def test_full_size_sampled(A, idx):
     w = W.D256_WORKLOADS[idx]
