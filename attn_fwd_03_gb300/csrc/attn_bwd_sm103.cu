@@ -32,14 +32,19 @@
 //   warp 11     idle
 //
 // Tensor memory (512 columns, lane = key row for S^T/dP^T/dK/dV, query row for dQ):
-//   [0,128)    S^T fp32; P^T bf16 pairs in [0,32) and [64,96) (see packed_col);
-//              then dQ columns 0-63 in [64,128)
+//   [0,128)    S^T fp32; P^T bf16 pairs in [0,32) and [64,96) (see packed_col)
 //   [128,256)  dP^T fp32; dS^T bf16 pairs in [128,160) and [192,224);
-//              then dQ columns 64-127 in [192,256)
-// The dQ MMAs overwrite packed P^T / dS^T columns only after the dV / dK MMAs
-// that read them: tcgen05 MMAs issued by one thread execute in order.
+//              then the dQ tile (columns 0-63 in [128,192), 64-127 in [192,256))
 //   [256,256+D)      dV accumulator
 //   [256+D,256+2D)   dK accumulator
+// The dQ MMAs overwrite packed dS^T columns, and the next tile's S^T MMAs packed P^T
+// columns, only after the dV / dK MMAs that read them: tcgen05 MMAs issued by one thread
+// execute in order. So the next tile's S^T runs while the warpgroups read the dQ tile out
+// of tensor memory; only its dP^T waits for them.
+//
+// The warpgroups hand over P^T / dS^T in two steps, one per 32-query chunk each of them
+// has packed, and the dV / dK products of the first chunks run while the second ones are
+// computed.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -94,7 +99,8 @@ struct BwdParamsDev {
 struct __align__(8) BwdBarriers {
     uint64_t kv_full;
     uint64_t st_full[2], st_empty[2];
-    uint64_t s_full, ds_ready, dq_full, dq_empty, kv_done;
+    uint64_t s_full, dq_full, dq_empty, kv_done;
+    uint64_t ds_ready[2];   // P^T / dS^T of chunk step cc (query chunks cc and 2 + cc) packed
     uint64_t dq_staged[2];  // two stages: per stage, the dQ tile staged in it for the TMA reduction;
                             // one stage: [0] a warpgroup's half staged in the separate area
     uint64_t stg_free;      // one stage: the separate area read by the last reduction
@@ -174,7 +180,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(&bar.stg_free, 1);
         mbar_init(&bar.s_full, 1);
-        mbar_init(&bar.ds_ready, 256);
+        mbar_init(&bar.ds_ready[0], 256);
+        mbar_init(&bar.ds_ready[1], 256);
         mbar_init(&bar.dq_full, 1);
         mbar_init(&bar.dq_empty, 256);
         mbar_init(&bar.kv_done, 1);
@@ -250,10 +257,6 @@ __global__ void __launch_bounds__(384, 1)
             const int s = it % Cfg::kStages;
             ok = mbar_wait_warp(&bar.st_full[s], (it / Cfg::kStages) & 1, wc);
             if (!ok) break;
-            if (it > 0) {  // S^T / dP^T overwrite the previous dQ tile
-                ok = mbar_wait_warp(&bar.dq_empty, (it - 1) & 1, wc);
-                if (!ok) break;
-            }
             tc_fence_after();
             const uint32_t sQ = smem_u32(smem + Cfg::kStageOff + s * Cfg::kStageBytes);
             const uint32_t sdO = sQ + Cfg::kTileBytes;
@@ -261,29 +264,50 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 0, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), kIdescS, kk > 0 ? 1u : 0u);
+            }
+            __syncwarp();
+            if (it > 0) {  // dP^T overwrites the previous dQ tile
+                ok = mbar_wait_warp(&bar.dq_empty, (it - 1) & 1, wc);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 128, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), kIdescS, kk > 0 ? 1u : 0u);
                 mma_commit(&bar.s_full);
             }
             __syncwarp();
-            ok = mbar_wait_warp(&bar.ds_ready, it & 1, wc);
+            // dV += P^T dO and dK += dS^T Q, 16 queries per k-step: chunk step cc brings the
+            // k-steps of query chunks cc and 2 + cc (2 k-steps each)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                ok = mbar_wait_warp(&bar.ds_ready[cc], it & 1, wc);
+                if (!ok) break;
+                tc_fence_after();
+                if (elect_one()) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int kk = 4 * (j >> 1) + 2 * cc + (j & 1);
+                        mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), kIdescKV,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int kk = 4 * (j >> 1) + 2 * cc + (j & 1);
+                        mma_ts(tmem + 256 + D, tmem + 128 + packed_col_k(kk), mnmajor_desc(sQ, kk), kIdescKV,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                __syncwarp();
+            }
             if (!ok) break;
-            tc_fence_after();
             if (elect_one()) {
-#pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), kIdescKV,
-                           (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    mma_ts(tmem + 256 + D, tmem + 128 + packed_col_k(kk), mnmajor_desc(sQ, kk), kIdescKV,
-                           (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int half = 0; half < D / 64; ++half)
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_ss(tmem + (half == 0 ? 64 : 192), mnmajor_desc(sDS, kk),
+                        mma_ss(tmem + 128 + 64 * half, mnmajor_desc(sDS, kk),
                                mnmajor_desc(sK + half * 128 * 128, kk), kIdescQ, kk > 0 ? 1u : 0u);
                 mma_commit(&bar.dq_full);
                 mma_commit(&bar.st_empty[s]);
@@ -347,7 +371,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t tRow = tmem + lane_off;
         uint8_t* ds_row = smem + Cfg::kDSOff + kr * 128;
         constexpr int kDqCols = D / 2;                                      // dQ columns per warpgroup
-        const uint32_t tDq = tRow + (D == 128 ? 64 + 128 * g : 64 + 32 * g);  // their TMEM columns
+        const uint32_t tDq = tRow + 128 + kDqCols * g;                       // their TMEM columns
         const float2 c2 = make_float2(p.c, p.c);
         bool ok = true;
         for (int it = 0; it < n_it && ok; ++it) {
@@ -405,11 +429,11 @@ __global__ void __launch_bounds__(384, 1)
                     *reinterpret_cast<uint4*>(box + ((ch ^ (kr & 7)) << 4)) =
                         make_uint4(dk[4 * j], dk[4 * j + 1], dk[4 * j + 2], dk[4 * j + 3]);
                 }
+                tmem_wait_st();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bar.ds_ready[cc]);
             }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bar.ds_ready);
 
             // dQ drain: this warpgroup's half of the columns of the dQ tile (thread = query row)
             ok = mbar_wait(&bar.dq_full, it & 1, wc);
