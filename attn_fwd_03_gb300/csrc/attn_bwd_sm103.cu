@@ -42,9 +42,10 @@
 // execute in order. So the next tile's S^T runs while the warpgroups read the dQ tile out
 // of tensor memory; only its dP^T waits for them.
 //
-// The warpgroups hand over P^T / dS^T in two steps, one per 32-query chunk each of them
-// has packed, and the dV / dK products of the first chunks run while the second ones are
-// computed.
+// S^T and dP^T complete separately, so the warpgroups compute the first chunk's P^T while
+// the dP^T product runs. They hand over P^T / dS^T in two steps, one per 32-query chunk each
+// of them has packed, and the dV / dK products of the first chunks run while the second ones
+// are computed.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -99,7 +100,7 @@ struct BwdParamsDev {
 struct __align__(8) BwdBarriers {
     uint64_t kv_full;
     uint64_t st_full[2], st_empty[2];
-    uint64_t s_full, dq_full, dq_empty, kv_done;
+    uint64_t s_full, dp_full, dq_full, dq_empty, kv_done;  // s_full: S^T done; dp_full: dP^T done
     uint64_t ds_ready[2];   // P^T / dS^T of chunk step cc (query chunks cc and 2 + cc) packed
     uint64_t dq_staged[2];  // two stages: per stage, the dQ tile staged in it for the TMA reduction;
                             // one stage: [0] a warpgroup's half staged in the separate area
@@ -180,6 +181,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         mbar_init(&bar.stg_free, 1);
         mbar_init(&bar.s_full, 1);
+        mbar_init(&bar.dp_full, 1);
         mbar_init(&bar.ds_ready[0], 256);
         mbar_init(&bar.ds_ready[1], 256);
         mbar_init(&bar.dq_full, 1);
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 0, kmajor_desc(sK, kk), kmajor_desc(sQ, kk), kIdescS, kk > 0 ? 1u : 0u);
+                mma_commit(&bar.s_full);
             }
             __syncwarp();
             if (it > 0) {  // dP^T overwrites the previous dQ tile
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 128, kmajor_desc(sV, kk), kmajor_desc(sdO, kk), kIdescS, kk > 0 ? 1u : 0u);
-                mma_commit(&bar.s_full);
+                mma_commit(&bar.dp_full);
             }
             __syncwarp();
             // dV += P^T dO and dK += dS^T Q, 16 queries per k-step: chunk step cc brings the
@@ -392,16 +395,15 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = 2 * g + cc;  // 32-column chunk of the tile
-                uint32_t sv[32], pv[32];
+                uint32_t sv[32];
                 tmem_ld32(tRow + 32 * c, sv);
-                tmem_ld32(tRow + 128 + 32 * c, pv);
                 tmem_wait_ld();
+                float pr[32];
                 uint32_t pk[16], dk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     const int q = 32 * c + i;
                     const float2 nl = *reinterpret_cast<const float2*>(nlv + q);
-                    const float2 nd = *reinterpret_cast<const float2*>(ndv + q);
                     float2 x = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), c2, nl);
                     if (MASK) {
                         const int kb = kr >> 6, kc = (kr & 63) >> 3;
@@ -413,13 +415,27 @@ __global__ void __launch_bounds__(384, 1)
                     }
                     if (!key_ok || (diag && q < kr)) x.x = -INFINITY;
                     if (!key_ok || (diag && q + 1 < kr)) x.y = -INFINITY;
-                    const float2 pr = make_float2(ex2(x.x), ex2(x.y));
-                    const float2 ds =
-                        fmul2(pr, fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd));
-                    pk[i / 2] = pack_h16<F16>(pr.x, pr.y);
-                    dk[i / 2] = pack_h16<F16>(ds.x, ds.y);
+                    pr[i] = ex2(x.x);
+                    pr[i + 1] = ex2(x.y);
+                    pk[i / 2] = pack_h16<F16>(pr[i], pr[i + 1]);
                 }
                 tmem_st16(tRow + packed_col(c), pk);
+                if (cc == 0) {  // the dP^T product runs while the first chunk's P^T is computed
+                    ok = mbar_wait(&bar.dp_full, it & 1, wc);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                uint32_t pv[32];
+                tmem_ld32(tRow + 128 + 32 * c, pv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float2 nd = *reinterpret_cast<const float2*>(ndv + 32 * c + i);
+                    const float2 ds = fmul2(make_float2(pr[i], pr[i + 1]),
+                                            fadd2(make_float2(__uint_as_float(pv[i]), __uint_as_float(pv[i + 1])), nd));
+                    dk[i / 2] = pack_h16<F16>(ds.x, ds.y);
+                }
                 tmem_st16(tRow + 128 + packed_col(c), dk);
                 // dS row kr, queries 32c .. 32c+31 -> box (32c / 64), chunks ((32c % 64) / 8) .. +3
                 uint8_t* box = ds_row + ((32 * c) >> 6) * (128 * 128);
@@ -434,6 +450,7 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 mbar_arrive(&bar.ds_ready[cc]);
             }
+            if (!ok) break;
 
             // dQ drain: this warpgroup's half of the columns of the dQ tile (thread = query row)
             ok = mbar_wait(&bar.dq_full, it & 1, wc);
