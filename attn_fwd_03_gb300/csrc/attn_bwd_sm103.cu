@@ -34,7 +34,7 @@
 // Tensor memory (512 columns, lane = key row for S^T/dP^T/dK/dV, query row for dQ):
 //   [0,128)    S^T fp32; P^T bf16 pairs in [0,32) and [64,96) (see packed_col)
 //   [128,256)  dP^T fp32; dS^T bf16 pairs in [128,160) and [192,224);
-//              then the dQ tile (columns 0-63 in [128,192), 64-127 in [192,256))
+//              then the dQ tile
 //   [256,256+D)      dV accumulator
 //   [256+D,256+2D)   dK accumulator
 // The dQ MMAs overwrite packed dS^T columns, and the next tile's S^T MMAs packed P^T
@@ -99,11 +99,13 @@ struct BwdParamsDev {
 
 struct __align__(8) BwdBarriers {
     uint64_t kv_full;
-    uint64_t st_full[2], st_empty[2];
+    uint64_t st_full[2], st_empty[2];  // per stage: Q, the statistics (and the mask tile)
+    uint64_t do_full[2], do_empty[2];  // per stage: dO
     uint64_t s_full, dp_full, dq_full, dq_empty, kv_done;  // s_full: S^T done; dp_full: dP^T done
     uint64_t ds_ready[2];   // P^T / dS^T of chunk step cc (query chunks cc and 2 + cc) packed
-    uint64_t dq_staged[2];  // two stages: per stage, the dQ tile staged in it for the TMA reduction;
-                            // one stage: [0] a warpgroup's half staged in the separate area
+    uint64_t dq_staged[2][2];  // two stages: per stage and warpgroup, its half of the dQ tile staged in
+                               // the stage's Q (warpgroup 0) or dO (warpgroup 1) area for the TMA
+                               // reduction; one stage: [0][0] a warpgroup's half in the separate area
     uint64_t stg_free;      // one stage: the separate area read by the last reduction
     uint64_t drain;
     uint32_t tmem_base;
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(384, 1)
     // 16-bit element type of the operands and of P^T, dS^T: bf16, or IEEE half when F16
     constexpr uint32_t kIdescS = idesc_h16(BK, BQ, false, false, F16);  // S^T, dP^T
     constexpr uint32_t kIdescKV = idesc_h16(BK, D, false, true, F16);   // dV, dK (A in TMEM)
-    constexpr uint32_t kIdescQ = idesc_h16(BQ, 64, true, true, F16);    // dQ half (A = dS query-major)
+    constexpr uint32_t kIdescQ = idesc_h16(BQ, D, true, true, F16);     // dQ (A = dS query-major)
     // dQ leaves through shared memory and TMA reductions. With two stages the current
     // stage's Q/dO area holds the whole tile (the next tile's operands sit in the other
     // stage); with one stage, staging there would hold up the next tile's load, so the
@@ -174,10 +176,13 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(&bar.kv_full, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar.st_full[s], 1);
-            // with two stages a stage is also the dQ staging area: free after the tile's MMAs
-            // and after the TMA reduction has read the staged dQ
+            mbar_init(&bar.do_full[s], 1);
+            // with two stages a stage is also the dQ staging area: its Q and dO areas are free
+            // after the tile's MMAs and after the TMA reduction has read the half staged there
             mbar_init(&bar.st_empty[s], kStageDq ? 2 : 1);
-            mbar_init(&bar.dq_staged[s], kStageDq ? 256 : 128);
+            mbar_init(&bar.do_empty[s], kStageDq ? 2 : 1);
+            mbar_init(&bar.dq_staged[s][0], 128);
+            mbar_init(&bar.dq_staged[s][1], 128);
         }
         mbar_init(&bar.stg_free, 1);
         mbar_init(&bar.s_full, 1);
@@ -229,11 +234,9 @@ __global__ void __launch_bounds__(384, 1)
             const int q0 = (i_begin + it) * BQ;
             uint8_t* st = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
             if (elect_one()) {
-                mbar_arrive_expect_tx(&bar.st_full[s], Cfg::kStageBytes);
-                for (int bx = 0; bx < Cfg::kBoxes; ++bx) {
+                mbar_arrive_expect_tx(&bar.st_full[s], Cfg::kStageBytes - Cfg::kTileBytes);
+                for (int bx = 0; bx < Cfg::kBoxes; ++bx)
                     tma_load_4d(st + bx * 128 * 128, &tm_q, &bar.st_full[s], bx * 64, q0, h, b);
-                    tma_load_4d(st + Cfg::kTileBytes + bx * 128 * 128, &tm_do, &bar.st_full[s], bx * 64, q0, h, b);
-                }
                 if (MASK)
                     for (int bx = 0; bx < 2; ++bx)
                         tma_load_4d(st + 2 * Cfg::kTileBytes + bx * 128 * 128, &tm_mask, &bar.st_full[s],
@@ -243,11 +246,22 @@ __global__ void __launch_bounds__(384, 1)
                           &bar.st_full[s]);
             }
             __syncwarp();
+            // dO: its area may be freed later than Q's (the dQ half staged there is reduced second)
+            ok = mbar_wait_warp(&bar.do_empty[s], ((it / Cfg::kStages) & 1) ^ 1, wc);
+            if (!ok) break;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(&bar.do_full[s], Cfg::kTileBytes);
+                for (int bx = 0; bx < Cfg::kBoxes; ++bx)
+                    tma_load_4d(st + Cfg::kTileBytes + bx * 128 * 128, &tm_do, &bar.do_full[s], bx * 64, q0, h, b);
+            }
+            __syncwarp();
         }
         if (lane == 0) {
             const int last = it < Cfg::kStages ? it : Cfg::kStages;
-            for (int i = it - last; i < it; ++i)
+            for (int i = it - last; i < it; ++i) {
                 drain_wait(&bar.st_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
+                drain_wait(&bar.do_full[i % Cfg::kStages], (i / Cfg::kStages) & 1, p.timeout_ns);
+            }
             drain_wait(&bar.kv_full, 0, p.timeout_ns);
         }
     } else if (warp == 9) {
@@ -272,8 +286,10 @@ __global__ void __launch_bounds__(384, 1)
             if (it > 0) {  // dP^T overwrites the previous dQ tile
                 ok = mbar_wait_warp(&bar.dq_empty, (it - 1) & 1, wc);
                 if (!ok) break;
-                tc_fence_after();
             }
+            ok = mbar_wait_warp(&bar.do_full[s], (it / Cfg::kStages) & 1, wc);
+            if (!ok) break;
+            tc_fence_after();
             if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
@@ -307,13 +323,11 @@ __global__ void __launch_bounds__(384, 1)
             if (!ok) break;
             if (elect_one()) {
 #pragma unroll
-                for (int half = 0; half < D / 64; ++half)
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        mma_ss(tmem + 128 + 64 * half, mnmajor_desc(sDS, kk),
-                               mnmajor_desc(sK + half * 128 * 128, kk), kIdescQ, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < BK / 16; ++kk)  // N = D: K read head-dim-major across its 64-column boxes
+                    mma_ss(tmem + 128, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), kIdescQ, kk > 0 ? 1u : 0u);
                 mma_commit(&bar.dq_full);
                 mma_commit(&bar.st_empty[s]);
+                mma_commit(&bar.do_empty[s]);
             }
             __syncwarp();
         }
@@ -336,19 +350,23 @@ __global__ void __launch_bounds__(384, 1)
             for (int it = 0; it < n_it && ok; ++it) {
                 const int q0 = (i_begin + it) * BQ;
                 if constexpr (kStageDq) {
+                    // warpgroup 0's half (Q area) first: the next load into the stage is Q's
                     const int s = it % Cfg::kStages;
-                    ok = mbar_wait(&bar.dq_staged[s], (it / Cfg::kStages) & 1, wc);
-                    if (!ok) break;
                     const uint8_t* stg = smem + Cfg::kStageOff + s * Cfg::kStageBytes;
+                    for (int g = 0; g < 2 && ok; ++g) {
+                        ok = mbar_wait(&bar.dq_staged[s][g], (it / Cfg::kStages) & 1, wc);
+                        if (!ok) break;
 #pragma unroll
-                    for (int bx = 0; bx < D / 32; ++bx)
-                        tma_reduce_add_4d(&tm_dq, stg + bx * (BQ * 128), 32 * bx, q0, h, b);
-                    bulk_commit();
-                    bulk_wait_read0();
-                    mbar_arrive(&bar.st_empty[s]);
+                        for (int bx = 0; bx < D / 64; ++bx)
+                            tma_reduce_add_4d(&tm_dq, stg + (g * (D / 64) + bx) * (BQ * 128), g * (D / 2) + 32 * bx,
+                                              q0, h, b);
+                        bulk_commit();
+                        bulk_wait_read0();
+                        mbar_arrive(g == 0 ? &bar.st_empty[s] : &bar.do_empty[s]);
+                    }
                 } else {
                     for (int g = 0; g < 2 && ok; ++g) {  // staging use k = 2 it + g
-                        ok = mbar_wait(&bar.dq_staged[0], g, wc);
+                        ok = mbar_wait(&bar.dq_staged[0][0], g, wc);
                         if (!ok) break;
                         const uint8_t* stg = smem + Cfg::kStgOff;
 #pragma unroll
@@ -492,7 +510,7 @@ __global__ void __launch_bounds__(384, 1)
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bar.dq_staged[kStageDq ? s : 0]);
+            mbar_arrive(kStageDq ? &bar.dq_staged[s][g] : &bar.dq_staged[0][0]);
         }
         // epilogue: warpgroup 0 writes the dV rows, warpgroup 1 the scale * dK rows of this key tile
         if (ok) ok = mbar_wait(&bar.kv_done, 0, wc);
