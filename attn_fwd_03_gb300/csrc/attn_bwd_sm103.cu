@@ -102,6 +102,7 @@ struct __align__(8) BwdBarriers {
     uint64_t st_full[2], st_empty[2];  // per stage: Q, the statistics (and the mask tile)
     uint64_t do_full[2], do_empty[2];  // per stage: dO
     uint64_t s_full, dp_full, dq_full, dq_empty, kv_done;  // s_full: S^T done; dp_full: dP^T done
+    uint64_t dv_done;  // the tile's last dV products (the last readers of its dO) done
     uint64_t ds_ready[2];   // P^T / dS^T of chunk step cc (query chunks cc and 2 + cc) packed
     uint64_t dq_staged[2][2];  // two stages: per stage and warpgroup, its half of the dQ tile staged in
                                // the stage's Q (warpgroup 0) or dO (warpgroup 1) area for the TMA
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_init(&bar.stg_free, 1);
         mbar_init(&bar.s_full, 1);
         mbar_init(&bar.dp_full, 1);
+        mbar_init(&bar.dv_done, 1);
         mbar_init(&bar.ds_ready[0], 256);
         mbar_init(&bar.ds_ready[1], 256);
         mbar_init(&bar.dq_full, 1);
@@ -305,11 +307,15 @@ __global__ void __launch_bounds__(384, 1)
                 if (!ok) break;
                 tc_fence_after();
                 if (elect_one()) {
+                    // the second chunks' dV products run after dQ (below), so that the dQ
+                    // tile's drain overlaps products that read only one operand from shared memory
+                    if (cc == 0) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int kk = 4 * (j >> 1) + 2 * cc + (j & 1);
-                        mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), kIdescKV,
-                               (it > 0 || kk > 0) ? 1u : 0u);
+                        for (int j = 0; j < 4; ++j) {
+                            const int kk = 4 * (j >> 1) + (j & 1);
+                            mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), kIdescKV,
+                                   (it > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -327,6 +333,13 @@ __global__ void __launch_bounds__(384, 1)
                     mma_ss(tmem + 128, mnmajor_desc(sDS, kk), mnmajor_desc(sK, kk), kIdescQ, kk > 0 ? 1u : 0u);
                 mma_commit(&bar.dq_full);
                 mma_commit(&bar.st_empty[s]);
+                // dV of the second chunks (P^T stays in the S^T columns, which dQ does not touch)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int kk = 4 * (j >> 1) + 2 + (j & 1);
+                    mma_ts(tmem + 256, tmem + packed_col_k(kk), mnmajor_desc(sdO, kk), kIdescKV, 1u);
+                }
+                mma_commit(&bar.dv_done);
                 mma_commit(&bar.do_empty[s]);
             }
             __syncwarp();
@@ -487,6 +500,11 @@ __global__ void __launch_bounds__(384, 1)
             uint8_t* stg;
             if constexpr (kStageDq) {
                 stg = smem + Cfg::kStageOff + s * Cfg::kStageBytes + g * (kDqCols / 32) * (BQ * 128);
+                if (g == 1) {  // the dO area: its last products (dV of the second chunks) follow dQ
+                    ok = mbar_wait(&bar.dv_done, it & 1, wc);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
             } else {
                 stg = smem + Cfg::kStgOff;
                 const int k = 2 * it + g;  // staging use; wait for use k-1 to have been read
