@@ -82,6 +82,14 @@ def test_committed_entries_name_existing_sources_and_summaries():
         assert os.path.exists(os.path.join(bench.ROOT, e["summary"])), e["summary"]
 
 
+def test_default_workload_dominant_kernel_traffic_is_current():
+    # the default benchmark line reports the backward main kernel's DRAM traffic only while the
+    # capture matches the committed sources: a kernel edit without a new capture fails here
+    w = bench.W.WORKLOADS[5]
+    kernel = "bwd_tc64_kernel" if w.d == 64 else "bwd_tc_kernel"
+    assert bench.captured_traffic(kernel, w.name) is not None
+
+
 def _clock_line(sm, mx=2070, hw="Not Active", hwt="Not Active", swt="Not Active", cap="Not Active"):
     return f"0, {sm}, {mx}, 812.5, 0x0000000000000000, {hw}, {hwt}, {swt}, {cap}"
 
